@@ -1,0 +1,507 @@
+"""Pins for the CPU oracle: checks that fix its results by something other than itself.
+
+Each ``pin_*`` function takes an ``oracle.Oracle`` and raises ``AssertionError`` when the oracle
+disagrees with a value fixed by hand, a closed form, an invariant of the method, a library
+routine (torch's bfloat16 rounding, numpy float64 sums, decimal's correctly rounded exp) or
+brute force on tiny inputs. ``test_oracle_pins.py`` runs them against the real oracle;
+``test_oracle_mutants.py`` runs them against copies of the oracle with a planted mistake and
+requires each copy to fail at least one pin.
+
+The method (sdm_decode_step docstring, decode.py; gather_cuda.py module docstring): per stream,
+with d = exp(g):  retrieved = sum_w kv_w d_w bank[k_w];  delta = beta (v - retrieved);
+bank[k_w] = d_w bank[k_w] + kv_w delta;  readings = sum_r qv_r bank[q_r] after the write.
+kv, v and qv are rounded to the bank dtype. The gather: out_o[t] = sum_n w[t,n] bank[idx[t,n]];
+stash = raw rows of operand 0; padding tokens give zeros.
+"""
+
+from __future__ import annotations
+
+import decimal
+import fractions
+import math
+
+import numpy as np
+import torch
+
+F32_EPS = 2.0 ** -24  # unit roundoff of float32
+
+
+# ---------------------------------------------------------------- helpers (no method arithmetic)
+
+def bf16_bits_torch(x) -> np.ndarray:
+    """float32 -> bf16 bits through torch's own conversion (round to nearest even)."""
+    t = torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).to(torch.bfloat16)
+    return t.view(torch.int16).numpy().view(np.uint16).copy()
+
+
+def bf16_bits_to_f32(b) -> np.ndarray:
+    b = np.ascontiguousarray(b, dtype=np.uint16)
+    return (b.astype(np.uint32) << 16).view(np.float32)
+
+
+def to_bank(x, dtype: str) -> np.ndarray:
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    return bf16_bits_torch(x) if dtype == "bf16" else x.copy()
+
+
+def bank_f32(b) -> np.ndarray:
+    return bf16_bits_to_f32(b) if b.dtype == np.uint16 else np.asarray(b, dtype=np.float32)
+
+
+def round_like_bank(x, dtype: str) -> np.ndarray:
+    """float32 values rounded to the bank dtype (torch's RNE) and widened back."""
+    return bank_f32(to_bank(x, dtype))
+
+
+def f32_nearest(q: fractions.Fraction) -> np.float32:
+    """The float32 nearest to the rational q (ties to even), for normal-range q."""
+    if q == 0:
+        return np.float32(0.0)
+    sign = -1 if q < 0 else 1
+    q = abs(q)
+    e = q.numerator.bit_length() - q.denominator.bit_length()
+    if fractions.Fraction(2) ** e > q:
+        e -= 1
+    scaled = q / fractions.Fraction(2) ** (e - 23)  # in [2^23, 2^24)
+    m = math.floor(scaled)
+    rem = scaled - m
+    if rem > fractions.Fraction(1, 2) or (rem == fractions.Fraction(1, 2) and m % 2 == 1):
+        m += 1
+    return np.float32(sign * float(fractions.Fraction(m) * fractions.Fraction(2) ** (e - 23)))
+
+
+def f32_exp_nearest(g: np.float32) -> np.float32:
+    """float32 nearest to e^g, from decimal's correctly rounded exp at 60 digits."""
+    ctx = decimal.Context(prec=60)
+    val = ctx.exp(decimal.Decimal(float(g)))
+    return f32_nearest(fractions.Fraction(val))
+
+
+def ordered_bf16(b) -> np.ndarray:
+    """bf16 bits mapped to integers in value order (+0 and -0 both map to 0)."""
+    b = np.asarray(b, dtype=np.uint16).astype(np.int64)
+    mag = b & 0x7FFF
+    return np.where(b & 0x8000, -mag, mag)
+
+
+def random_decode_case(rng: np.random.Generator, dtype: str, S: int, P: int, hd: int, W: int, R: int, G: int,
+                       T: int = 1, idx=np.int32, kq_scale: float = 0.35):
+    """Small random decode inputs: stream s owns slots [s*P, (s+1)*P); W distinct write slots."""
+    bank = to_bank(rng.normal(0.0, 0.5, size=(S * P, hd)), dtype)
+    k_idx = np.stack([np.stack([rng.choice(P, size=W, replace=False) + s * P for s in range(S)]) for _ in range(T)])
+    q_idx = rng.integers(0, P, size=(T, S, R)) + (np.arange(S) * P)[None, :, None]
+    f = np.float32
+    return dict(bank=bank, k_idx=k_idx.astype(idx), k_val=(rng.normal(size=(T, S, W)) * kq_scale).astype(f),
+                v=rng.normal(size=(T, S, hd)).astype(f), beta=(1 / (1 + np.exp(-rng.normal(size=(T, S))))).astype(f),
+                g=(-np.log1p(np.exp(rng.normal(size=(T, S, G))))).astype(f), q_idx=q_idx.astype(idx),
+                q_val=(rng.normal(size=(T, S, R)) * kq_scale).astype(f))
+
+
+def run_seq(orc, case, bank=None):
+    bank = case["bank"].copy() if bank is None else bank
+    out = orc.decode_seq(bank, case["k_idx"], case["k_val"], case["v"], case["beta"], case["g"], case["q_idx"],
+                         case["q_val"])
+    return bank, out
+
+
+def hand_step(orc, dtype, bank, k_idx, k_val, v, beta, g, q_idx, q_val):
+    """One stream, one token, from plain Python lists; returns (bank after, readings) as float32."""
+    f = np.float32
+    bank_arr = to_bank(np.array(bank, dtype=f), dtype)
+    out = orc.decode_step(bank_arr, np.array([k_idx], np.int64), np.array([k_val], f), np.array([v], f),
+                          np.array([beta], f), np.array([g], f), np.array([q_idx], np.int64), np.array([q_val], f))
+    return bank_f32(bank_arr), bank_f32(out)[0]
+
+
+def assert_bits_equal(a, b, what: str):
+    a = np.asarray(a)
+    b = np.asarray(b)
+    assert a.shape == b.shape, f"{what}: shape {a.shape} vs {b.shape}"
+    av = a.view(np.uint32) if a.dtype == np.float32 else a
+    bv = b.view(np.uint32) if b.dtype == np.float32 else b
+    bad = np.flatnonzero(av.ravel() != bv.ravel())
+    assert bad.size == 0, f"{what}: {bad.size} elements differ, first at {bad[0]}: {a.ravel()[bad[0]]} vs {b.ravel()[bad[0]]}"
+
+
+# ---------------------------------------------------------------- bf16 rounding
+
+
+def pin_bf16_rounding_matches_torch(orc):
+    """The oracle's float32 -> bf16 equals torch's round-to-nearest-even, ties included."""
+    rng = np.random.default_rng(1)
+    x = np.concatenate([rng.normal(size=20000) * 10.0 ** rng.integers(-30, 30, size=20000),
+                        [0.0, -0.0, 1.0, -1.0, np.inf, -np.inf, 3.4028235e38, -3.4028235e38, 1e-45, 1.1754944e-38]])
+    x = x.astype(np.float32)
+    # exact ties: a bf16 value plus half its ulp (low half = 0x8000)
+    b = rng.integers(0, 0x7F00, size=5000).astype(np.uint32)
+    ties = ((b << 16) | 0x8000).view(np.float32)
+    x = np.concatenate([x, ties, -ties])
+    assert_bits_equal(orc.f32_to_bf16(x), bf16_bits_torch(x), "f32->bf16")
+    assert_bits_equal(orc.bf16_to_f32(bf16_bits_torch(x)), bf16_bits_to_f32(bf16_bits_torch(x)), "bf16->f32")
+    nan = orc.f32_to_bf16(np.array([np.nan], np.float32))
+    assert np.isnan(bf16_bits_to_f32(nan)[0])
+
+
+# ---------------------------------------------------------------- decode: hand cases (exact dyadics)
+
+
+def pin_hand_fp32_w1(orc):
+    """bank rows [1,-0.5],[0.25,2]; write slot 0 with kv=0.5, d=1, beta=0.5, v=[2,1]; read slot 0 x2.
+    retrieved = 0.5*[1,-0.5] = [0.5,-0.25]; delta = 0.5*([2,1]-[0.5,-0.25]) = [0.75,0.625];
+    new row = [1,-0.5] + 0.5*[0.75,0.625] = [1.375,-0.1875]; readings = 2*new = [2.75,-0.375]."""
+    bank, out = hand_step(orc, "f32", [[1.0, -0.5], [0.25, 2.0]], [0], [0.5], [2.0, 1.0], 0.5, [0.0], [0], [2.0])
+    assert bank.tolist() == [[1.375, -0.1875], [0.25, 2.0]]
+    assert out.tolist() == [2.75, -0.375]
+
+
+def pin_hand_fp32_w2(orc):
+    """Slots s0=[1,2,-1], s1=[0.5,0,4], s2=[-2,1,0.25], s3=[3,3,3]; writes (s2, kv=1), (s0, kv=-0.5);
+    d=1, beta=0.25, v=[0,1,2]; reads (s0, 2), (s3, -1).
+    retrieved = s2 - 0.5 s0 = [-2.5,0,0.75]; delta = 0.25*(v - retrieved) = [0.625,0.25,0.3125];
+    s2' = s2 + delta = [-1.375,1.25,0.5625]; s0' = s0 - 0.5 delta = [0.6875,1.875,-1.15625];
+    readings = 2 s0' - s3 = [-1.625,0.75,-5.3125]."""
+    bank, out = hand_step(orc, "f32", [[1, 2, -1], [0.5, 0, 4], [-2, 1, 0.25], [3, 3, 3]], [2, 0], [1.0, -0.5],
+                          [0, 1, 2], 0.25, [0.0], [0, 3], [2.0, -1.0])
+    assert bank.tolist() == [[0.6875, 1.875, -1.15625], [0.5, 0, 4], [-1.375, 1.25, 0.5625], [3, 3, 3]]
+    assert out.tolist() == [-1.625, 0.75, -5.3125]
+
+
+def pin_hand_fp32_two_streams_w3(orc):
+    """Two streams, hd=1, G=W (all gates 0), stream 0 owns slots 0-3 and stream 1 slots 4-7.
+    bank = [1,2,3,4,-1,-2,-3,-4].
+    Stream 0: writes (3,.5),(1,.25),(0,1), beta=1, v=10: retrieved = 2+0.5+1 = 3.5, delta = 6.5,
+      s3'=4+3.25=7.25, s1'=2+1.625=3.625, s0'=1+6.5=7.5; reads (0,1),(0,.5),(2,-2): 7.5+3.75-6 = 5.25.
+    Stream 1: writes (4,-1),(6,.5),(5,.5), beta=.5, v=0: retrieved = 1-1.5-1 = -1.5, delta = 0.75,
+      s4'=-1.75, s6'=-2.625, s5'=-1.625; reads (7,.25),(4,1),(6,-1): -1-1.75+2.625 = -0.125."""
+    f = np.float32
+    bank = np.array([[1], [2], [3], [4], [-1], [-2], [-3], [-4]], f)
+    out = orc.decode_step(bank, np.array([[3, 1, 0], [4, 6, 5]], np.int32), np.array([[.5, .25, 1], [-1, .5, .5]], f),
+                          np.array([[10], [0]], f), np.array([1, .5], f), np.zeros((2, 3), f),
+                          np.array([[0, 0, 2], [7, 4, 6]], np.int32), np.array([[1, .5, -2], [.25, 1, -1]], f))
+    assert bank.ravel().tolist() == [7.5, 3.625, 3, 7.25, -1.75, -1.625, -2.625, -4]
+    assert out.ravel().tolist() == [5.25, -0.125]
+
+
+def pin_hand_seq_two_tokens(orc):
+    """One stream, hd=1, bank [1,2].
+    Token 0: write (0, kv=1), beta=.5, v=3: retrieved=1, delta=1, s0'=2; read (1, 1) -> 2.
+    Token 1: write (1, kv=2), beta=.25, v=0: retrieved=4, delta=-1, s1'=2-2=0; read (0,-1) -> -2,
+    which uses token 0's write of s0."""
+    f = np.float32
+    bank = np.array([[1], [2]], f)
+    out = orc.decode_seq(bank, np.array([[[0]], [[1]]], np.int64), np.array([[[1]], [[2]]], f),
+                         np.array([[[3]], [[0]]], f), np.array([[.5], [.25]], f), np.zeros((2, 1, 1), f),
+                         np.array([[[1]], [[0]]], np.int64), np.array([[[1]], [[-1]]], f))
+    assert bank.ravel().tolist() == [2, 0]
+    assert out.ravel().tolist() == [2, -2]
+
+
+def pin_hand_bf16_q_rounding(orc):
+    """bf16 bank, reads of s0=1 and s1=-1 with qv = 0.5+2^-9+2^-11 and 0.5. The first weight
+    rounds to bf16 0.5+2^-8 (0.625 ulp above 0.5), so readings = 2^-8 (unrounded it would be
+    2^-9+2^-11). The write (slot 2, kv=0) leaves s2 = 0.5."""
+    bank, out = hand_step(orc, "bf16", [[1.0], [-1.0], [0.5]], [2], [0.0], [0.0], 0.0, [0.0], [0, 1],
+                          [0.5 + 2 ** -9 + 2 ** -11, 0.5])
+    assert out.tolist() == [2.0 ** -8]
+    assert bank.ravel().tolist() == [1.0, -1.0, 0.5]
+
+
+def pin_hand_bf16_v_rounding(orc):
+    """bf16 bank, zero row, kv=1, d=1, beta=0.75, v = 2+2^-7+2^-9: v rounds to 2+2^-6 (0.625 ulp up),
+    delta = 0.75*2.015625 = 1.51171875, exactly halfway between bf16 1.5078125 and 1.515625; ties
+    to even give 1.515625 (unrounded v would give 1.5073 -> 1.5078125). Read of the slot: 1.515625."""
+    bank, out = hand_step(orc, "bf16", [[0.0]], [0], [1.0], [2 + 2 ** -7 + 2 ** -9], 0.75, [0.0], [0], [1.0])
+    assert bank.ravel().tolist() == [1.515625]
+    assert out.tolist() == [1.515625]
+
+
+def pin_hand_bf16_k_rounding(orc):
+    """bf16 bank, s0=1, kv = 1+2^-8+2^-10 rounds to 1+2^-7; d=1, beta=1, v=0:
+    retrieved = kv, delta = -kv, s0' = 1 - kv^2 = -(2^-6 + 2^-14) in float32, a bf16 tie that
+    rounds to even: -2^-6. (Unrounded kv would give -0.0097656.) Read of s0: -2^-6."""
+    bank, out = hand_step(orc, "bf16", [[1.0]], [0], [1 + 2 ** -8 + 2 ** -10], [0.0], 1.0, [0.0], [0], [1.0])
+    assert bank.ravel().tolist() == [-(2.0 ** -6)]
+    assert out.tolist() == [-(2.0 ** -6)]
+
+
+# ---------------------------------------------------------------- decode: invariants and closed forms
+
+
+def pin_identity_update(orc):
+    """beta=0, g=0: every write stores d*row + kv*0 = row, so the bank stays bit-identical (zero-free
+    bank); readings are the plain weighted sum of the old rows (numpy float64, then rounded)."""
+    rng = np.random.default_rng(2)
+    for dtype in ("f32", "bf16"):
+        case = random_decode_case(rng, dtype, S=3, P=40, hd=16, W=8, R=8, G=1)
+        case["beta"][:] = 0.0
+        case["g"][:] = 0.0
+        assert np.all(bank_f32(case["bank"]) != 0.0)
+        bank0 = case["bank"].copy()
+        bank, out = run_seq(orc, case)
+        assert_bits_equal(bank, bank0, f"{dtype} bank after beta=0")
+        rows = bank_f32(bank0).astype(np.float64)[case["q_idx"][0]]  # [S, R, hd]
+        qv = round_like_bank(case["q_val"][0], dtype).astype(np.float64)
+        ref = np.einsum("sr,src->sc", qv, rows)
+        got = bank_f32(out[0]).astype(np.float64)
+        if dtype == "f32":
+            bound = 8 * F32_EPS * np.einsum("sr,src->sc", np.abs(qv), np.abs(rows)) + 1e-30
+            assert np.all(np.abs(got - ref) <= bound)
+        else:
+            dist = np.abs(ordered_bf16(out[0]) - ordered_bf16(to_bank(ref.astype(np.float32), "bf16")))
+            assert dist.max() <= 1
+
+
+def pin_overwrite(orc):
+    """W=1, kv=1, g=0, beta=1: the written row becomes v. For bf16 banks the float32 difference and
+    sum are exact, so the row equals bf16(v) bit for bit; for float32 banks with row and v within a
+    factor of two (Sterbenz) it is exact too."""
+    rng = np.random.default_rng(3)
+    for dtype in ("bf16", "f32"):
+        case = random_decode_case(rng, dtype, S=4, P=16, hd=24, W=1, R=1, G=1)
+        case["k_val"][:] = 1.0
+        case["g"][:] = 0.0
+        case["beta"][:] = 1.0
+        rows = case["k_idx"][0, :, 0]
+        if dtype == "f32":
+            mag = rng.uniform(1.0, 1.9, size=(4, 24)).astype(np.float32)
+            sign = np.where(rng.random((4, 24)) < 0.5, -1.0, 1.0).astype(np.float32)
+            case["bank"][rows] = mag * sign
+            case["v"][0] = (mag * rng.uniform(0.55, 1.0, size=(4, 24)) * sign).astype(np.float32)
+        bank, _ = run_seq(orc, case)
+        assert_bits_equal(bank[rows], to_bank(case["v"][0], dtype), f"{dtype} overwrite")
+
+
+def pin_read_after_write(orc):
+    """A read of a slot written in the same step sees the new row: R=1, q=k[0], qv=1 gives the new
+    row exactly. A read of a slot no write touched gives the old row exactly."""
+    rng = np.random.default_rng(4)
+    for dtype in ("bf16", "f32"):
+        case = random_decode_case(rng, dtype, S=3, P=32, hd=20, W=4, R=1, G=1)
+        case["q_idx"][0, :, 0] = case["k_idx"][0, :, 0]
+        case["q_val"][:] = 1.0
+        bank, out = run_seq(orc, case)
+        assert_bits_equal(out[0], bank[case["k_idx"][0, :, 0]], f"{dtype} read after write")
+        case2 = random_decode_case(rng, dtype, S=3, P=32, hd=20, W=4, R=1, G=1)
+        for s in range(3):
+            free = sorted(set(range(s * 32, s * 32 + 32)) - set(case2["k_idx"][0, s].tolist()))
+            case2["q_idx"][0, s, 0] = free[0]
+        case2["q_val"][:] = 1.0
+        bank0 = case2["bank"].copy()
+        _, out2 = run_seq(orc, case2)
+        assert_bits_equal(out2[0], bank0[case2["q_idx"][0, :, 0]], f"{dtype} read of an untouched slot")
+
+
+def pin_decay_only(orc):
+    """beta=0 with per-write gates (G=W): each written row becomes round(row * d_w) where d_w is the
+    float32 nearest to e^{g_w} (decimal exp), and the product is one float32 multiply."""
+    rng = np.random.default_rng(5)
+    for dtype in ("f32", "bf16"):
+        case = random_decode_case(rng, dtype, S=2, P=24, hd=12, W=6, R=2, G=6)
+        case["beta"][:] = 0.0
+        bank0 = bank_f32(case["bank"]).copy()
+        bank, _ = run_seq(orc, case)
+        for s in range(2):
+            for w in range(6):
+                d = f32_exp_nearest(case["g"][0, s, w])
+                slot = case["k_idx"][0, s, w]
+                ref = (bank0[slot] * d).astype(np.float32)
+                assert_bits_equal(bank[slot], to_bank(ref, dtype), f"{dtype} decay of slot {slot}")
+
+
+def pin_gate_sharing(orc):
+    """G=1 and G=W with every per-write gate equal to the shared gate give identical bits."""
+    rng = np.random.default_rng(6)
+    for dtype in ("f32", "bf16"):
+        case = random_decode_case(rng, dtype, S=3, P=30, hd=10, W=5, R=7, G=1, T=3)
+        case_w = dict(case)
+        case_w["g"] = np.repeat(case["g"], 5, axis=2).copy()
+        b1, o1 = run_seq(orc, case)
+        b2, o2 = run_seq(orc, case_w)
+        assert_bits_equal(b1, b2, f"{dtype} bank G=1 vs G=W")
+        assert_bits_equal(o1, o2, f"{dtype} readings G=1 vs G=W")
+
+
+def pin_delta_rule_projection(orc):
+    """Reading back with the write key (q = k, same weights) after a write returns
+    r + beta ||k||^2 (v - r), with r = d sum_w kv_w row_w: the delta rule's defining property.
+    Checked for float32 banks against a float64 evaluation of that closed form."""
+    rng = np.random.default_rng(7)
+    case = random_decode_case(rng, "f32", S=5, P=64, hd=16, W=8, R=8, G=1)
+    case["q_idx"] = case["k_idx"].copy()
+    case["q_val"] = case["k_val"].copy()
+    bank0 = case["bank"].astype(np.float64)
+    _, out = run_seq(orc, case)
+    kv = case["k_val"][0].astype(np.float64)
+    d = np.exp(case["g"][0, :, 0].astype(np.float64))
+    rows = bank0[case["k_idx"][0]]  # [S, W, hd]
+    r = d[:, None] * np.einsum("sw,swc->sc", kv, rows)
+    beta = case["beta"][0].astype(np.float64)[:, None]
+    ref = r + beta * (kv ** 2).sum(1)[:, None] * (case["v"][0].astype(np.float64) - r)
+    got = out[0].astype(np.float64)
+    assert np.all(np.abs(got - ref) <= 1e-5 * (1 + np.abs(ref))), np.abs(got - ref).max()
+    # a unit key (four weights of 0.5), d = 1, beta = 1: the read returns v
+    case["k_val"][:] = 0.0
+    case["k_val"][0, :, :4] = 0.5
+    case["q_val"] = case["k_val"].copy()
+    case["g"][:] = 0.0
+    case["beta"][:] = 1.0
+    _, out = run_seq(orc, case)
+    assert np.all(np.abs(out[0] - case["v"][0]) <= 1e-5 * (1 + np.abs(case["v"][0])))
+
+
+def pin_column_independence(orc):
+    """Columns never mix: running the two column halves as separate banks gives the same bits."""
+    rng = np.random.default_rng(8)
+    for dtype in ("f32", "bf16"):
+        case = random_decode_case(rng, dtype, S=2, P=20, hd=8, W=4, R=4, G=4, T=2)
+        bank, out = run_seq(orc, case)
+        for lo, hi in ((0, 3), (3, 8)):
+            part = dict(case)
+            part["bank"] = np.ascontiguousarray(case["bank"][:, lo:hi])
+            part["v"] = np.ascontiguousarray(case["v"][:, :, lo:hi])
+            pb, po = run_seq(orc, part)
+            assert_bits_equal(pb, bank[:, lo:hi], f"{dtype} bank columns {lo}:{hi}")
+            assert_bits_equal(po, out[:, :, lo:hi], f"{dtype} readings columns {lo}:{hi}")
+
+
+def pin_stream_independence(orc):
+    """Changing stream 1's inputs leaves stream 0's readings and slots bit-unchanged."""
+    rng = np.random.default_rng(9)
+    case = random_decode_case(rng, "bf16", S=2, P=16, hd=6, W=3, R=3, G=1, T=2)
+    b1, o1 = run_seq(orc, case)
+    case2 = {k: v.copy() for k, v in case.items()}
+    case2["v"][:, 1] += 1.0
+    case2["k_val"][:, 1] *= -1.0
+    case2["beta"][:, 1] = 0.5
+    b2, o2 = run_seq(orc, case2)
+    assert_bits_equal(o1[:, 0], o2[:, 0], "stream 0 readings")
+    assert_bits_equal(b1[:16], b2[:16], "stream 0 slots")
+    assert not np.array_equal(o1[:, 1], o2[:, 1])
+
+
+def pin_seq_equals_steps(orc):
+    """T tokens in one multi-token call equal T single-token calls in order."""
+    rng = np.random.default_rng(10)
+    case = random_decode_case(rng, "bf16", S=3, P=12, hd=9, W=4, R=5, G=4, T=4, idx=np.int64)
+    b1, o1 = run_seq(orc, case)
+    bank = case["bank"].copy()
+    for t in range(4):
+        o = orc.decode_step(bank, case["k_idx"][t], case["k_val"][t], case["v"][t], case["beta"][t], case["g"][t],
+                            case["q_idx"][t], case["q_val"][t])
+        assert_bits_equal(o, o1[t], f"token {t}")
+    assert_bits_equal(bank, b1, "bank")
+
+
+def pin_contract_checks(orc):
+    """Duplicate write slots and out-of-range slots are reported; bad widths are argument errors."""
+    import oracle as _o
+    rng = np.random.default_rng(11)
+    case = random_decode_case(rng, "f32", S=1, P=8, hd=2, W=3, R=1, G=1)
+    dup = {k: v.copy() for k, v in case.items()}
+    dup["k_idx"][0, 0, 1] = dup["k_idx"][0, 0, 0]
+    for bad, rc in ((dup, _o.EDUP),):
+        try:
+            run_seq(orc, bad)
+        except _o.OracleError as e:
+            assert e.rc == rc
+        else:
+            raise AssertionError("duplicate write slots not reported")
+    far = {k: v.copy() for k, v in case.items()}
+    far["q_idx"][0, 0, 0] = 8
+    try:
+        run_seq(orc, far)
+    except _o.OracleError as e:
+        assert e.rc == _o.ERANGE
+    else:
+        raise AssertionError("out-of-range read slot not reported")
+
+
+# ---------------------------------------------------------------- gather
+
+
+def pin_gather_hand(orc):
+    """float32 bank rows r0=[1,2], r1=[0.5,-1], r2=[4,0.25]; 2 tokens, chunk 2, valid 1.
+    Token 0: op0 (r2, 0.5), (r0, -1) -> [2-1, 0.125-2] = [1, -1.875]; op1 (r1, 2) -> [1, -2];
+    stash = [r2, r0]. Token 1 is padding: zero outputs and zero stash rows."""
+    f = np.float32
+    bank = np.array([[1, 2], [0.5, -1], [4, 0.25]], f)
+    out0, out1, st = orc.gather(bank, np.array([[2, 0], [1, 1]], np.int32), np.array([[.5, -1], [3, 3]], f),
+                                np.array([[1], [0]], np.int32), np.array([[2], [5]], f), chunk=2, valid=1)
+    assert out0.tolist() == [[1, -1.875], [0, 0]]
+    assert out1.tolist() == [[1, -2], [0, 0]]
+    assert st.tolist() == [[[4, 0.25], [1, 2]], [[0, 0], [0, 0]]]
+
+
+def pin_gather_group_order(orc):
+    """Entries x = [1, 2^-24, 0, 2^-24] (weights 1). One chain: 1 + 2^-24 ties to 1, twice -> 1.
+    Two interleaved groups {x0,x2}, {x1,x3}: partials 1 and 2^-23, sum 1 + 2^-23. (Two blocked
+    groups {x0,x1}, {x2,x3} would give 1.) Four groups: 0+1+2^-24+0+2^-24 -> 1."""
+    f = np.float32
+    bank = np.array([[1.0], [2.0 ** -24], [0.0], [2.0 ** -24]], f)
+    idx = np.array([[0, 1, 2, 3]], np.int32)
+    w = np.ones((1, 4), f)
+    expect = {1: 1.0, 2: 1.0 + 2.0 ** -23, 4: 1.0}
+    for groups, val in expect.items():
+        out0, _, _ = orc.gather(bank, idx, w, chunk=1, groups=groups, stash=False)
+        assert out0[0, 0] == np.float32(val), (groups, out0[0, 0])
+
+
+def _random_gather(rng, dtype: str, wdtype: str, n_slots=50, hd=12, tokens=12, chunk=4, widths=(7, 5)):
+    bank = to_bank(rng.normal(size=(n_slots, hd)), dtype)
+    ops = []
+    for width in widths:
+        idx = rng.integers(0, n_slots, size=(tokens, width)).astype(np.int64)
+        w = rng.normal(size=(tokens, width)).astype(np.float32) * 0.5
+        ops.append((idx, to_bank(w, wdtype)))
+    cv = rng.integers(0, chunk + 1, size=tokens // chunk).astype(np.int32)
+    return bank, ops, cv
+
+
+def pin_gather_library(orc):
+    """Outputs against a float64 einsum over the gathered rows (error within the float32 bound for
+    sequential summation, gamma_n sum |w x|); stash rows equal numpy's fancy indexing bit for bit;
+    padding tokens (per-chunk valid) give zero outputs and zero stash rows."""
+    rng = np.random.default_rng(12)
+    for dtype, wdtype in (("bf16", "bf16"), ("f32", "f32"), ("bf16", "f32"), ("f32", "bf16")):
+        bank, ops, cv = _random_gather(rng, dtype, wdtype)
+        (i0, w0), (i1, w1) = ops
+        out0, out1, st = orc.gather(bank, i0, w0, i1, w1, chunk=4, chunk_valid=cv)
+        live = (np.arange(12) % 4) < np.repeat(cv, 4)
+        bf = bank_f32(bank).astype(np.float64)
+        for idx, w, out in ((i0, w0, out0), (i1, w1, out1)):
+            wf = bank_f32(w).astype(np.float64)
+            ref = np.einsum("tn,tnc->tc", wf, bf[idx])
+            bound = idx.shape[1] * F32_EPS * np.einsum("tn,tnc->tc", np.abs(wf), np.abs(bf[idx])) * 1.01
+            assert np.all(np.abs(out[live] - ref[live]) <= bound[live])
+            assert np.all(out[~live] == 0) and not np.any(np.signbit(out[~live]))
+        assert_bits_equal(st[live], bank[i0[live]], f"{dtype} stash rows")
+        assert np.all(st[~live] == 0)
+
+
+def pin_gather_one_hot(orc):
+    """A single weight of one (others zero) copies the selected row exactly into the output."""
+    rng = np.random.default_rng(13)
+    for dtype in ("bf16", "f32"):
+        bank, ops, _ = _random_gather(rng, dtype, dtype, widths=(6,))
+        idx, _ = ops[0]
+        w = np.zeros((12, 6), np.float32)
+        hot = rng.integers(0, 6, size=12)
+        w[np.arange(12), hot] = 1.0
+        out0, _, _ = orc.gather(bank, idx, to_bank(w, dtype), chunk=4)
+        assert_bits_equal(out0, bank_f32(bank)[idx[np.arange(12), hot]], f"{dtype} one-hot")
+
+
+def pin_gather_scaling(orc):
+    """Doubling every weight doubles every output exactly (power-of-two scaling commutes with
+    rounding), and valid = 0 makes every token padding."""
+    rng = np.random.default_rng(14)
+    bank, ops, _ = _random_gather(rng, "bf16", "f32", widths=(9,))
+    idx, w = ops[0]
+    a, _, _ = orc.gather(bank, idx, w, chunk=4)
+    b, _, _ = orc.gather(bank, idx, (w * 2).astype(np.float32), chunk=4)
+    assert_bits_equal(b, (a * 2).astype(np.float32), "doubled weights")
+    z, _, st = orc.gather(bank, idx, w, chunk=4, valid=0)
+    assert np.all(z == 0) and np.all(st == 0)
+
+
+ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_") and callable(v)]
