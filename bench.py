@@ -1,0 +1,531 @@
+#!/usr/bin/env python
+"""Benchmark of the SDM decode hot path on GB300.
+
+A step is one sdm_decode_seq launch over the serving-scale decode workload: 1024 streams (batch 64
+x 16 heads), head_dim 128, a bf16 bank of 16384 private slots per stream (4 GiB), W = R = 64
+writes and reads per token, one gate per token, int32 slots, T = 64 tokens per stream.
+The metric is stream-tokens per second (whole job over all ranks) with the effective bank
+bandwidth as a fraction of the measured HBM peak.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--no-extras]
+
+--impl reference times the CPU oracle on the host cores instead (the reference arm: bounded
+samples of the same workload per step). Under torch.distributed.run every rank runs its own
+shard (weak scaling); rank 0 prints one JSON line.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from decode_state_gb300 import dist as sdist  # noqa: E402
+from decode_state_gb300 import workloads  # noqa: E402
+
+METRIC = "SDM stream-tokens/sec and effective bank GB/s as fraction of GB300 HBM peak"
+UNIT = "stream-tokens/s"
+WL = workloads.C2
+DECODE_KEYS = ("k_idx", "k_val", "v", "beta", "g", "q_idx", "q_val")
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse_args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=1000)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    p.add_argument("--no-extras", action="store_true", help="skip the secondary workloads")
+    p.add_argument("--cpu-seconds", type=float, default=10.0, help="oracle time budget of the CPU baseline")
+    p.add_argument("--workload", default=WL.name,
+                   choices=sorted(list(workloads.DECODE_WORKLOADS) + list(workloads.GATHER_WORKLOADS)),
+                   help="workload of the timed step (default: the serving-scale decode)")
+    p.add_argument("--streams", type=int, default=0, help="override the decode stream count (smaller cases)")
+    p.add_argument("--tokens", type=int, default=0, help="override T (decode) or the token count (gather)")
+    a = p.parse_args()
+    a.warmup = max(3, a.warmup)
+    a.steps = max(1, a.steps)
+    return a
+
+
+# ---------------------------------------------------------------- peaks, clocks, profiles
+
+
+def hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "decode_state_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(f.encode() + b"\0" + fh.read())
+    return h.hexdigest()
+
+
+def ncu_traffic(workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on the current kernels."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f).get(workload)
+    except (OSError, ValueError):
+        return None
+    if not rec or rec.get("kernel_source_sha256") != kernel_source_hash():
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clock and throttle-reason samples (100 ms) with host timestamps."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device: torch.device):
+        self.samples = []
+        self.proc = None
+        self.error = None
+        try:
+            props = torch.cuda.get_device_properties(device)
+            bus = f"{props.pci_domain_id:08X}:{props.pci_bus_id:02X}:{props.pci_device_id:02X}.0"
+            sel = ["-i", bus]
+        except Exception:  # older torch: no PCI ids
+            sel = []
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-lms", "100", *sel], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+        except OSError as e:
+            self.error = f"nvidia-smi unavailable: {e}"
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                self.samples.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0: float, t1: float):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "note": self.error}
+        inside = [p for (t, p) in self.samples if t0 <= t <= t1]
+        note = None
+        if len(inside) < 3:  # a short timed region: use the samples around it too
+            inside = [p for (t, p) in self.samples if t0 - 0.5 <= t <= t1 + 0.5]
+            note = "few samples inside the timed region; includes samples within 0.5 s of it"
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+
+        sm = [num(p[1]) for p in inside if num(p[1]) is not None]
+        mx = [num(p[2]) for p in inside if num(p[2]) is not None]
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        reasons = sorted({n for p in inside for n, v in zip(names, p[5:9]) if v.lower() == "active"})
+        out = {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+               "reasons": reasons, "samples": len(inside)}
+        if note:
+            out["note"] = note
+        return out
+
+
+# ---------------------------------------------------------------- workloads as timed cases
+
+
+def _np(t):
+    import numpy as np
+
+    t = t.detach().cpu().contiguous()
+    if t.dtype == torch.bfloat16:
+        return t.view(torch.int16).numpy().view(np.uint16).copy()
+    return t.numpy().copy()
+
+
+def oracle_stream_tokens(x: dict, streams, P: int):
+    """Oracle run over whole streams of a decode workload (host copies); returns (stream-tokens, seconds)."""
+    import oracle
+
+    orc = oracle.default()
+    done, secs = 0, 0.0
+    for s in streams:
+        args = []
+        for k in DECODE_KEYS:
+            v = x[k][:, s:s + 1]
+            args.append(_np(v - s * P if k in ("k_idx", "q_idx") else v))
+        bank = _np(x["bank"][s * P:(s + 1) * P])
+        t0 = time.perf_counter()
+        orc.decode_seq(bank, *args, check=False)
+        secs += time.perf_counter() - t0
+        done += x["k_idx"].shape[0]
+    return done, secs
+
+
+def oracle_gather_tokens(bank_h, g: dict, tokens, chunk: int):
+    """Oracle run over a list of gather tokens (host copies); returns (tokens, seconds)."""
+    import oracle
+
+    orc = oracle.default()
+    tok = torch.as_tensor(tokens, dtype=torch.int64)
+    (i0, w0), *rest = g["ops"]
+    a = [_np(i0[tok]), _np(w0[tok])]
+    if rest:
+        a += [_np(rest[0][0][tok]), _np(rest[0][1][tok])]
+    cv = g["chunk_valid"]
+    valid_t = (cv[tok // chunk] if cv is not None else torch.full((len(tokens),), chunk, dtype=torch.int32))
+    # one token per chunk of one: a live token has valid 1, a padding token valid 0
+    per_token = _np(((tok % chunk) < valid_t.cpu().to(torch.int64)).to(torch.int32))
+    t0 = time.perf_counter()
+    orc.gather(bank_h, *a, chunk=1, chunk_valid=per_token, check=False)
+    return len(tokens), time.perf_counter() - t0
+
+
+class Case:
+    """One timed workload: its step, its units and bytes, its end-to-end form and its oracle."""
+
+    def __init__(self, args, dev, r: sdist.Rank):
+        from decode_state_gb300 import sdm
+
+        self.sdm = sdm
+        name = args.workload
+        self.dev = dev
+        if name in workloads.DECODE_WORKLOADS:
+            wl = workloads.DECODE_WORKLOADS[name]
+            if args.streams:
+                wl = wl.scaled(n_streams=args.streams)
+            if args.tokens:
+                wl = wl.scaled(T=args.tokens)
+            self.kind = "decode_" + wl.mode
+            self.x = workloads.make_decode_inputs(wl, device=dev, seed=sdist.shard_seed(wl.seed, r))
+            bdt = workloads.BANK_DTYPES[wl.bank_dtype]
+            self.out = torch.empty((wl.T, wl.n_streams, wl.hd), dtype=bdt, device=dev)
+            self.units = wl.n_streams * wl.T
+            self.unit = UNIT
+            self.launches = 1 if wl.mode == "seq" else wl.T
+            self.nbytes = workloads.decode_bytes_per_stream_token(wl) * wl.n_streams * wl.T
+            self.kernel = f"decode_kernel<{wl.bank_dtype},{wl.idx_dtype},bulk>"
+            self.metric = METRIC
+        else:
+            wl = workloads.GATHER_WORKLOADS[name]
+            if args.tokens:
+                wl = wl.scaled(tokens=args.tokens)
+            self.kind = "gather"
+            self.g = workloads.make_gather_inputs(wl, device=dev, seed=sdist.shard_seed(wl.seed, r))
+            self.outs = [torch.empty((wl.tokens, wl.hd), device=dev) for _ in wl.widths]
+            bdt = workloads.BANK_DTYPES[wl.bank_dtype]
+            self.stash = (torch.empty((wl.tokens, wl.widths[0], wl.hd), dtype=bdt, device=dev) if wl.stash else None)
+            self.units = wl.tokens
+            self.unit = "tokens/s"
+            self.launches = 1
+            self.nbytes = workloads.gather_bytes(wl, self.g["chunk_valid"])
+            self.kernel = f"gather_kernel<{wl.bank_dtype},{wl.idx_dtype},{wl.w_dtype},bulk>"
+            self.metric = "SDM token-gather tokens/sec and effective bank GB/s as fraction of GB300 HBM peak"
+        self.wl = wl
+
+    # device-resident step
+    def step(self):
+        wl, sdm = self.wl, self.sdm
+        if self.kind == "decode_seq":
+            sdm.decode_seq(self.x["bank"], *(self.x[k] for k in DECODE_KEYS), out=self.out)
+        elif self.kind == "decode_step":
+            for t in range(wl.T):
+                sdm.decode_step(self.x["bank"], *(self.x[k][t] for k in DECODE_KEYS), out=self.out[t])
+        else:
+            sdm.gather(self.g["bank"], self.g["ops"], chunk=wl.chunk, chunk_valid=self.g["chunk_valid"],
+                       stash=self.stash, outs=self.outs, with_stash=self.stash is not None)
+
+    def config(self, r: sdist.Rank) -> dict:
+        wl = self.wl
+        par = f"weak: {r.world} independent shard(s), no collective in the data path"
+        if self.kind == "gather":
+            return {"workload": wl.name, "n_slots": wl.n_slots, "head_dim": wl.hd, "tokens": wl.tokens,
+                    "chunk": wl.chunk, "widths": list(wl.widths), "bank_dtype": wl.bank_dtype,
+                    "idx_dtype": wl.idx_dtype, "w_dtype": wl.w_dtype, "stash": wl.stash, "call": "sdm_gather",
+                    "l2": "inputs larger than L2 (1 GiB bank), no flush", "parallelism": par}
+        bank_gib = wl.n_slots * wl.hd * (2 if wl.bank_dtype == "bf16" else 4) / 2 ** 30
+        return {"workload": wl.name, "streams": wl.n_streams, "head_dim": wl.hd,
+                "slots_per_stream": wl.slots_per_stream, "W": wl.W, "R": wl.R, "G": wl.G, "T": wl.T,
+                "bank_dtype": wl.bank_dtype, "idx_dtype": wl.idx_dtype,
+                "call": "sdm_decode_seq" if self.kind == "decode_seq" else "sdm_decode_step x T",
+                "l2": (f"inputs larger than L2 ({bank_gib:.2f} GiB bank), no flush" if bank_gib > 0.2 else
+                       f"L2-resident ({bank_gib * 1024:.0f} MiB bank)"), "parallelism": par}
+
+    # end to end: host inputs in, results out, every step
+    def e2e(self, steps: int, r: sdist.Rank) -> dict:
+        dev, wl, sdm = self.dev, self.wl, self.sdm
+        stream = torch.cuda.current_stream(dev)
+        if self.kind.startswith("decode"):
+            host_in = [self.x[k].cpu().pin_memory() for k in DECODE_KEYS]
+            dev_in = [torch.empty_like(self.x[k]) for k in DECODE_KEYS]
+            host_out = torch.empty(self.out.shape, dtype=self.out.dtype, pin_memory=True)
+            d2h = host_out.numel() * host_out.element_size()
+
+            def step():
+                for d, h in zip(dev_in, host_in):
+                    d.copy_(h, non_blocking=True)
+                if self.kind == "decode_seq":
+                    sdm.decode_seq(self.x["bank"], *dev_in, out=self.out)
+                else:
+                    for t in range(wl.T):
+                        sdm.decode_step(self.x["bank"], *(d[t] for d in dev_in), out=self.out[t])
+                host_out.copy_(self.out, non_blocking=True)
+        else:
+            g = self.g
+            flat = [t for op in g["ops"] for t in op] + ([g["chunk_valid"]] if g["chunk_valid"] is not None else [])
+            host_in = [t.cpu().pin_memory() for t in flat]
+            dev_in = [torch.empty_like(t) for t in flat]
+            host_outs = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in self.outs]
+            d2h = sum(o.numel() * o.element_size() for o in host_outs)
+            n_ops = len(g["ops"])
+
+            def step():
+                for d, h in zip(dev_in, host_in):
+                    d.copy_(h, non_blocking=True)
+                ops = [(dev_in[2 * o], dev_in[2 * o + 1]) for o in range(n_ops)]
+                cv = dev_in[2 * n_ops] if g["chunk_valid"] is not None else None
+                sdm.gather(g["bank"], ops, chunk=wl.chunk, chunk_valid=cv, stash=self.stash, outs=self.outs,
+                           with_stash=self.stash is not None)
+                for h, o in zip(host_outs, self.outs):
+                    h.copy_(o, non_blocking=True)
+        h2d = sum(t.numel() * t.element_size() for t in host_in)
+        for _ in range(3):
+            step()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        sdist.barrier(r, dev)
+        e0.record(stream)
+        for _ in range(steps):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms = sdist.max_over_ranks(r, e0.elapsed_time(e1), dev)
+        return {"value": self.units * steps * r.world / (ms / 1e3), "unit": self.unit, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": steps, "ms_per_step": ms / steps}
+
+    # the oracle on the host cores, on a time-bounded sample of this workload's own inputs
+    def cpu_baseline(self, budget_s: float) -> dict:
+        if self.kind.startswith("decode"):
+            S, P = self.wl.n_streams, self.wl.slots_per_stream
+            order = torch.randperm(S, generator=torch.Generator().manual_seed(0)).tolist()
+            done, secs, n = 0, 0.0, 0
+            for s in order:
+                d, t = oracle_stream_tokens(self.x, [s], P)
+                done, secs, n = done + d, secs + t, n + 1
+                if secs >= budget_s:
+                    break
+            sample = (f"{n} of {S} streams x {self.wl.T} tokens of the benchmark's own inputs "
+                      f"({done} stream-tokens, {secs:.1f} s single-threaded)")
+        else:
+            bank_h = _np(self.g["bank"])
+            order = torch.randperm(self.wl.tokens, generator=torch.Generator().manual_seed(0))
+            done, secs, i = 0, 0.0, 0
+            while secs < budget_s and i < self.wl.tokens:
+                d, t = oracle_gather_tokens(bank_h, self.g, order[i:i + 256].tolist(), self.wl.chunk)
+                done, secs, i = done + d, secs + t, i + 256
+            sample = (f"{done} of {self.wl.tokens} tokens of the benchmark's own inputs "
+                      f"(padding included, {secs:.1f} s single-threaded)")
+        return {"value": done / secs, "unit": self.unit, "cores": 1, "kind": "oracle", "sample": sample}
+
+
+# ---------------------------------------------------------------- our arm
+
+
+def run_ours(args, r: sdist.Rank):
+    from decode_state_gb300 import sdm
+
+    dev = torch.device("cuda", r.local_rank)
+    torch.cuda.set_device(dev)
+    sdm.library()
+    case = Case(args, dev, r)
+    for _ in range(args.warmup):
+        case.step()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream(dev)
+    sampler = ClockSampler(dev)
+    time.sleep(0.3)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sdist.barrier(r, dev)
+    torch.cuda.synchronize()
+    h0 = time.time()
+    e0.record(stream)
+    for a, b in ev:
+        a.record(stream)
+        case.step()
+        b.record(stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    h1 = time.time()
+    sdist.barrier(r, dev)
+    time.sleep(0.2)
+    sampler.stop()
+    elapsed_ms = e0.elapsed_time(e1)
+    step_ms = statistics.fmean(a.elapsed_time(b) for a, b in ev)
+    max_ms = sdist.max_over_ranks(r, elapsed_ms, dev)
+    value = case.units * args.steps * r.world / (max_ms / 1e3)
+    peak, peak_kind = hbm_peak()
+    launch_ms = step_ms / case.launches
+    achieved = case.nbytes / case.launches / (launch_ms / 1e3) / 1e9
+    res = {
+        "metric": case.metric, "value": value, "unit": case.unit, "n_gpus": r.world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": max_ms / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic", "config": case.config(r),
+        "effective_gbs": case.nbytes * args.steps * r.world / (max_ms / 1e3) / 1e9,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": ncu_traffic(case.wl.name), "peak_kind": peak_kind, "kernel": case.kernel,
+                     "algorithmic_bytes_per_launch": case.nbytes // case.launches, "avg_launch_ms": launch_ms},
+        "gpu_launches": args.steps * case.launches,
+        "clocks": sampler.summary(h0, h1),
+    }
+    res["e2e"] = case.e2e(max(3, min(args.steps, 200)), r)
+    res["device_status"] = sdm.device_status()
+    return res, case
+
+
+def _time_calls(fn, reps: int, warm: int = 3):
+    for _ in range(warm):
+        fn()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        fn()
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / reps
+
+
+def extras(args, dev, r: sdist.Rank, peak: float, skip: str):
+    """The other workloads (parity cases of the test suite), timed briefly for context."""
+    res = {}
+    for name in list(workloads.DECODE_WORKLOADS) + list(workloads.GATHER_WORKLOADS):
+        if name == skip or name == workloads.C0.name:
+            continue
+        a = argparse.Namespace(**vars(args))
+        a.workload, a.streams, a.tokens = name, 0, 0
+        case = Case(a, dev, r)
+        reps = 5 if case.kind == "decode_step" else 20
+        ms = _time_calls(case.step, reps)
+        item = {"unit_per_s": case.units / (ms / 1e3), "unit": case.unit, "ms_per_step": ms,
+                "effective_gbs": case.nbytes / (ms / 1e3) / 1e9, "frac_of_hbm_peak": case.nbytes / (ms / 1e3) / 1e9 / peak,
+                "launches_per_step": case.launches}
+        if case.kind == "decode_step":  # the same single-token launches replayed from a CUDA graph
+            graph = torch.cuda.CUDAGraph()
+            s = torch.cuda.Stream(dev)
+            s.wait_stream(torch.cuda.current_stream(dev))
+            with torch.cuda.stream(s):
+                case.step()
+                torch.cuda.synchronize()
+                with torch.cuda.graph(graph, stream=s):
+                    case.step()
+            torch.cuda.current_stream(dev).wait_stream(s)
+            gms = _time_calls(graph.replay, reps, 1)
+            item.update({"graph_unit_per_s": case.units / (gms / 1e3), "graph_ms_per_step": gms,
+                         "graph_us_per_launch": gms * 1e3 / case.launches})
+            del graph
+        res[name] = item
+        del case
+        torch.cuda.empty_cache()
+    return res
+
+
+# ---------------------------------------------------------------- reference arm (the oracle)
+
+
+def run_reference(args, r: sdist.Rank):
+    """The CPU oracle on the host cores: each step is the oracle over a bounded sample of whole
+    streams of the same workload (drawn on the host with the same generator recipe)."""
+    if args.workload not in workloads.DECODE_WORKLOADS:
+        raise SystemExit("--impl reference times the decode workloads")
+    base = workloads.DECODE_WORKLOADS[args.workload]
+    n_pool = min(8, base.n_streams)
+    wl = base.scaled(n_streams=n_pool)
+    x = workloads.make_decode_inputs(wl, device="cpu", seed=base.seed)
+    _, per_stream_s = oracle_stream_tokens(x, [0], wl.slots_per_stream)
+    total = args.steps + args.warmup
+    budget = 90.0
+    per_step_streams = max(1, min(n_pool, int(budget / total / max(per_stream_s, 1e-6))))
+    T_used = wl.T
+    if per_stream_s * total > budget:  # even one whole stream per step is too long: a prefix of its tokens
+        T_used = max(1, int(wl.T * budget / total / per_stream_s))
+    xs = {k: (v[:T_used] if k in DECODE_KEYS else v) for k, v in x.items()}
+
+    def step(i):
+        lo = (i * per_step_streams) % n_pool
+        return oracle_stream_tokens(xs, [(lo + j) % n_pool for j in range(per_step_streams)], wl.slots_per_stream)
+
+    for i in range(args.warmup):
+        step(i)
+    done, t0 = 0, time.perf_counter()
+    for i in range(args.steps):
+        done += step(i)[0]
+    secs = time.perf_counter() - t0
+    value = done / secs
+    sample = (f"{per_step_streams} whole stream(s) x {T_used} token(s) per step, cycling over {n_pool} streams "
+              f"drawn with the workload's recipe")
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": r.world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs * 1e3 / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": base.name, "streams": base.n_streams, "head_dim": base.hd,
+                       "slots_per_stream": base.slots_per_stream, "W": base.W, "R": base.R, "G": base.G,
+                       "T": base.T, "bank_dtype": base.bank_dtype, "idx_dtype": base.idx_dtype,
+                       "call": "oracle_sdm_decode_seq"},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    args = parse_args()
+    r = sdist.init_from_env()
+    try:
+        if args.impl == "reference":
+            if r.is_root:
+                print(json.dumps(run_reference(args, r)), flush=True)
+            return
+        res, case = run_ours(args, r)
+        if r.is_root:
+            res["cpu_baseline"] = case.cpu_baseline(args.cpu_seconds)
+        del case
+        torch.cuda.empty_cache()
+        if r.is_root and r.world == 1 and not args.no_extras:
+            res["other_workloads"] = extras(args, torch.device("cuda", r.local_rank), r, res["roofline"]["peak"],
+                                            res["config"]["workload"])
+        if r.is_root:
+            print(json.dumps(res), flush=True)
+    finally:
+        sdist.shutdown(r)
+
+
+if __name__ == "__main__":
+    main()

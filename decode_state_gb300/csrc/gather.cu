@@ -1,0 +1,288 @@
+// SDM token gather.
+//
+// Math (sparse-delta-memory 2.0.0, cuda/gather_cuda.py, module docstring): for every token t and
+// operand o,
+//     out_o[t]    = sum_n w_o[t, n] * bank[idx_o[t, n]]     (float32 accumulation)
+//     stash[t, n] = bank[idx_0[t, n]]                       (raw rows of operand 0)
+// and a token whose position in its chunk is >= valid is padding: it reads nothing and gets zero
+// outputs and zero stash rows.
+//
+// Design. One block owns one (token, column slice). Warp 0 issues one bulk copy per entry row
+// slice (both operands, all in flight at once) into shared memory, completion counted on an
+// mbarrier; the stash rows then leave shared memory by bulk stores (one store for the whole
+// token when the slice is the full row) while each thread reduces its CPT columns over the
+// entries in ascending order with fmaf (the reference's order with one row group). Rows that
+// are not a multiple of 16 bytes, or an unaligned bank, take a plain-load path with one column
+// per thread. Row indices outside [0, n_slots) are skipped (zero row) and flagged in the status
+// word.
+#include <algorithm>
+#include <climits>
+
+#include "../../include/sdm.h"
+#include "sdm_device.cuh"
+#include "sdm_internal.h"
+
+namespace sdm {
+namespace {
+
+__device__ unsigned int g_gather_status;
+
+constexpr int kMaxThreads = 256;
+constexpr size_t kRowsBudget = 40 * 1024;
+
+__host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+struct GatherLayout {
+    size_t rows, slot, wt, bar, total;
+    __host__ __device__ GatherLayout(int n_rows, int slice_cols, int es) {
+        rows = 0;
+        slot = align_up((size_t)n_rows * slice_cols * es, 16);
+        wt = slot + (size_t)n_rows * 8;
+        bar = align_up(wt + (size_t)n_rows * 4, 8);
+        total = bar + 8;
+    }
+};
+
+template <typename WT>
+__device__ __forceinline__ float load_weight(const void* p, int64_t i) {
+    return to_f32(__ldg(static_cast<const WT*>(p) + i));
+}
+
+template <typename E, int CPT>
+__device__ __forceinline__ void read_staged(const E* p, float (&x)[CPT]) {
+    if constexpr (CPT == 2) {
+        const uint32_t u = *reinterpret_cast<const uint32_t*>(p);
+        x[0] = __uint_as_float(u << 16);
+        x[1] = __uint_as_float(u & 0xffff0000u);
+    } else {
+        x[0] = to_f32(p[0]);
+    }
+}
+
+// Zero this block's slice of the outputs and stash rows of padding token t.
+template <typename E, int CPT>
+__device__ void write_padding(const GatherArgs& a, int64_t t, int c0, int ncols, int j, bool active, bool flat16) {
+    const int hd = a.hd, W0 = a.width[0];
+    if (active) {
+#pragma unroll
+        for (int k = 0; k < CPT; ++k) a.out[0][t * hd + c0 + j + k] = 0.0f;
+        if (a.n_ops == 2)
+#pragma unroll
+            for (int k = 0; k < CPT; ++k) a.out[1][t * hd + c0 + j + k] = 0.0f;
+    }
+    if (a.stash == nullptr) return;
+    E* st = static_cast<E*>(a.stash) + t * W0 * hd;
+    if (flat16) {  // the token's whole stash block is contiguous and 16-byte aligned
+        uint4* p = reinterpret_cast<uint4*>(st);
+        const int n16 = (int)((size_t)W0 * hd * sizeof(E) / 16);
+        for (int i = threadIdx.x; i < n16; i += blockDim.x) p[i] = make_uint4(0u, 0u, 0u, 0u);
+    } else if (active) {
+        for (int n = 0; n < W0; ++n)
+#pragma unroll
+            for (int k = 0; k < CPT; ++k) st[(int64_t)n * hd + c0 + j + k] = E(0);
+    }
+}
+
+template <typename E, typename I, typename WT, bool BULK>
+__global__ void __launch_bounds__(kMaxThreads) gather_kernel(const GatherArgs a, int stash_bulk) {
+    constexpr int ES = sizeof(E);
+    constexpr int CPT = (BULK && ES == 2) ? 2 : 1;
+    extern __shared__ __align__(128) unsigned char smem[];
+    __shared__ int s_abort;
+
+    const int hd = a.hd, sw = a.slice_cols;
+    const int W0 = a.width[0], W1 = a.n_ops == 2 ? a.width[1] : 0, NR = W0 + W1;
+    const GatherLayout L(NR, sw, ES);
+    E* rows = reinterpret_cast<E*>(smem + L.rows);
+    int64_t* slot = reinterpret_cast<int64_t*>(smem + L.slot);
+    float* wt = reinterpret_cast<float*>(smem + L.wt);
+    uint64_t* bar = reinterpret_cast<uint64_t*>(smem + L.bar);
+
+    const int tid = threadIdx.x, nt = blockDim.x;
+    const int64_t t = blockIdx.x / a.n_slices;
+    const int c0 = (int)(blockIdx.x % a.n_slices) * sw;
+    const int ncols = min(sw, hd - c0);
+    const int j = tid * CPT;
+    const bool active = j < ncols;
+    const uint32_t row_bytes = (uint32_t)ncols * ES;
+    const E* bank = static_cast<const E*>(a.bank);
+    E* stash = static_cast<E*>(a.stash);
+
+    const int vt = a.chunk_valid != nullptr ? __ldg(a.chunk_valid + t / a.chunk) : a.valid;
+    if ((int)(t % a.chunk) >= vt) {
+        write_padding<E, CPT>(a, t, c0, ncols, j, active, stash_bulk && a.n_slices == 1);
+        return;
+    }
+
+    // entries of both operands: operand 0 in [0, W0), operand 1 in [W0, NR)
+    for (int e = tid; e < NR; e += nt) {
+        const bool op1 = e >= W0;
+        const int64_t i = op1 ? t * W1 + (e - W0) : t * W0 + e;
+        int64_t sl = load_index<I>(op1 ? a.idx[1] : a.idx[0], i);
+        if (sl < 0 || sl >= a.n_slots) {
+            atomicOr(&g_gather_status, SDM_DEV_BAD_INDEX);
+            sl = -1;
+        }
+        slot[e] = sl;
+        wt[e] = load_weight<WT>(op1 ? a.w[1] : a.w[0], i);
+    }
+    if (BULK && tid == 0) {
+        s_abort = 0;
+        mbar_init(bar, 1);
+        mbar_init_fence();
+    }
+    __syncthreads();
+
+    if (BULK) {
+        if (tid < 32) {
+            uint32_t bytes = 0;
+            for (int e = tid; e < NR; e += 32)
+                if (slot[e] >= 0) bytes += row_bytes;
+            if (bytes) mbar_expect_tx(bar, bytes);
+            for (int e = tid; e < NR; e += 32) {
+                if (slot[e] >= 0) {
+                    bulk_g2s(rows + (size_t)e * sw, bank + slot[e] * hd + c0, row_bytes, bar);
+                } else {
+                    for (int c = 0; c < ncols; ++c) rows[(size_t)e * sw + c] = E(0);
+                    fence_proxy_async_shared();
+                }
+            }
+            __syncwarp();
+            if (tid == 0) mbar_arrive(bar);
+        }
+        const bool ok = mbar_wait_bounded(bar, 0, kWaitLimitNs);
+        if (!ok) atomicOr(&s_abort, 1);
+        __syncthreads();
+        if (s_abort) {
+            if (tid == 0) atomicOr(&g_gather_status, SDM_DEV_TIMEOUT);
+            if (!ok) mbar_wait_bounded(bar, 0, kWaitLimitNs);
+            return;
+        }
+        // stash: raw rows of operand 0 straight from shared memory
+        if (stash != nullptr) {
+            if (stash_bulk) {
+                if (a.n_slices == 1) {
+                    if (tid == 0) {
+                        fence_proxy_async_shared();
+                        bulk_s2g(stash + t * W0 * hd, rows, (uint32_t)W0 * hd * ES);
+                        bulk_commit();
+                    }
+                } else if (tid < 32) {
+                    fence_proxy_async_shared();
+                    for (int n = tid; n < W0; n += 32)
+                        bulk_s2g(stash + (t * W0 + n) * hd + c0, rows + (size_t)n * sw, row_bytes);
+                    bulk_commit();
+                }
+            } else if (active) {
+                for (int n = 0; n < W0; ++n)
+#pragma unroll
+                    for (int k = 0; k < CPT; ++k)
+                        stash[(t * W0 + n) * hd + c0 + j + k] = rows[(size_t)n * sw + j + k];
+            }
+        }
+    } else if (active) {
+        // plain loads of this thread's column; the bank is read-only for the kernel's lifetime
+        int e = 0;
+        for (; e + 8 <= NR; e += 8) {
+            E x[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int64_t sl = slot[e + u];
+                x[u] = sl >= 0 ? __ldg(bank + sl * hd + c0 + j) : E(0);
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) rows[(size_t)(e + u) * sw + j] = x[u];
+        }
+        for (; e < NR; ++e) {
+            const int64_t sl = slot[e];
+            rows[(size_t)e * sw + j] = sl >= 0 ? __ldg(bank + sl * hd + c0 + j) : E(0);
+        }
+        if (stash != nullptr)
+            for (int n = 0; n < W0; ++n) stash[(t * W0 + n) * hd + c0 + j] = rows[(size_t)n * sw + j];
+    }
+
+    // weighted sums, one fmaf chain per column over ascending entries
+    if (active) {
+        for (int o = 0; o < a.n_ops; ++o) {
+            const int e0 = o ? W0 : 0, width = o ? W1 : W0;
+            float acc[CPT];
+#pragma unroll
+            for (int k = 0; k < CPT; ++k) acc[k] = 0.0f;
+            for (int n = 0; n < width; ++n) {
+                float x[CPT];
+                read_staged<E, CPT>(rows + (size_t)(e0 + n) * sw + j, x);
+                const float w = wt[e0 + n];
+#pragma unroll
+                for (int k = 0; k < CPT; ++k) acc[k] = fmaf(w, x[k], acc[k]);
+            }
+            float* dst = (o ? a.out[1] : a.out[0]) + t * hd + c0 + j;
+#pragma unroll
+            for (int k = 0; k < CPT; ++k) dst[k] = acc[k];
+        }
+    }
+    // shared memory must outlive the bulk stores that read it
+    if (BULK && stash != nullptr && stash_bulk && (a.n_slices == 1 ? tid == 0 : tid < 32)) bulk_wait_read_all();
+}
+
+template <typename E, typename I, typename WT>
+int launch_typed(bool bulk, const GatherArgs& a, int stash_bulk, dim3 grid, dim3 block, size_t smem,
+                 cudaStream_t stream) {
+    if (bulk)
+        gather_kernel<E, I, WT, true><<<grid, block, smem, stream>>>(a, stash_bulk);
+    else
+        gather_kernel<E, I, WT, false><<<grid, block, smem, stream>>>(a, stash_bulk);
+    return (int)cudaGetLastError();
+}
+
+template <typename E, typename I>
+int launch_w(int w_dtype, bool bulk, const GatherArgs& a, int stash_bulk, dim3 grid, dim3 block, size_t smem,
+             cudaStream_t stream) {
+    return w_dtype == SDM_BF16 ? launch_typed<E, I, uint16_t>(bulk, a, stash_bulk, grid, block, smem, stream)
+                               : launch_typed<E, I, float>(bulk, a, stash_bulk, grid, block, smem, stream);
+}
+
+int shrink_cols(int sw, bool bulk, int es) {
+    const int q = bulk ? 16 / es : 32;
+    const int half = (sw / 2 + q - 1) / q * q;
+    return std::max(q, half);
+}
+
+}  // namespace
+
+int launch_gather(const GatherArgs& a0, int bank_dtype, int idx_dtype, int w_dtype, cudaStream_t stream) {
+    GatherArgs a = a0;
+    if (a.tokens == 0) return 0;
+    const int es = bank_dtype == SDM_BF16 ? 2 : 4;
+    const bool bulk = ((int64_t)a.hd * es) % 16 == 0 && reinterpret_cast<uintptr_t>(a.bank) % 16 == 0;
+    const int cpt = (bulk && es == 2) ? 2 : 1;
+    const int n_rows = a.width[0] + (a.n_ops == 2 ? a.width[1] : 0);
+
+    int sw = std::min(a.hd, kMaxThreads * cpt);
+    if (bulk) sw = sw / (16 / es) * (16 / es);
+    while ((size_t)n_rows * sw * es > kRowsBudget && sw > (bulk ? 16 / es : 32)) sw = shrink_cols(sw, bulk, es);
+    a.slice_cols = sw;
+    a.n_slices = (a.hd + sw - 1) / sw;
+    const int64_t blocks = a.tokens * a.n_slices;
+    if (blocks > INT_MAX) return SDM_ECOUNT;
+    const int stash_bulk = a.stash != nullptr && reinterpret_cast<uintptr_t>(a.stash) % 16 == 0 && bulk;
+    const int threads = ((sw + cpt - 1) / cpt + 31) / 32 * 32;
+    const size_t smem = GatherLayout(n_rows, sw, es).total;
+    const dim3 grid((unsigned)blocks), block((unsigned)threads);
+    if (bank_dtype == SDM_BF16) {
+        return idx_dtype == SDM_I32 ? launch_w<uint16_t, int32_t>(w_dtype, bulk, a, stash_bulk, grid, block, smem, stream)
+                                    : launch_w<uint16_t, int64_t>(w_dtype, bulk, a, stash_bulk, grid, block, smem, stream);
+    }
+    return idx_dtype == SDM_I32 ? launch_w<float, int32_t>(w_dtype, bulk, a, stash_bulk, grid, block, smem, stream)
+                                : launch_w<float, int64_t>(w_dtype, bulk, a, stash_bulk, grid, block, smem, stream);
+}
+
+int gather_status(unsigned int* word, bool clear) {
+    cudaError_t e = cudaMemcpyFromSymbol(word, g_gather_status, sizeof(unsigned int));
+    if (e == cudaSuccess && clear) {
+        const unsigned int zero = 0;
+        e = cudaMemcpyToSymbol(g_gather_status, &zero, sizeof(unsigned int));
+    }
+    return (int)e;
+}
+
+}  // namespace sdm

@@ -1,0 +1,177 @@
+// C ABI of the SDM library: argument validation (host only, before any CUDA call) and dispatch to
+// the kernel files. Every entry point follows include/sdm.h: 0 = launched, < 0 = argument error,
+// > 0 = cudaError_t.
+#include <atomic>
+#include <climits>
+
+#include "../../include/sdm.h"
+#include "sdm_internal.h"
+
+namespace sdm {
+
+int sm_count() {
+    static std::atomic<int> cache[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return 148;
+    }
+    if (dev >= 0 && dev < 64) {
+        const int c = cache[dev].load(std::memory_order_relaxed);
+        if (c > 0) return c;
+    }
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+        (void)cudaGetLastError();
+        n = 148;
+    }
+    if (dev >= 0 && dev < 64) cache[dev].store(n, std::memory_order_relaxed);
+    return n;
+}
+
+}  // namespace sdm
+
+namespace {
+
+bool aligned(const void* p, size_t a) { return reinterpret_cast<uintptr_t>(p) % a == 0; }
+
+bool overlaps(const void* a, size_t an, const void* b, size_t bn) {
+    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return x < y + bn && y < x + an;
+}
+
+int check_decode(void* bank, const void* k_idx, const float* k_val, const float* v, const float* beta,
+                 const float* g, const void* q_idx, const float* q_val, void* out, int64_t n_streams, int hd, int W,
+                 int R, int G, int T, int bank_dtype, int idx_dtype) {
+    if (bank_dtype != SDM_BF16 && bank_dtype != SDM_F32) return SDM_EDTYPE;
+    if (idx_dtype != SDM_I32 && idx_dtype != SDM_I64) return SDM_EIDX;
+    if (hd < 1 || hd > 65536) return SDM_EHD;
+    if (W < 1 || W > 256 || R < 1 || R > 256) return SDM_EWIDTH;
+    if (G != 1 && G != W) return SDM_EGATES;
+    if (n_streams < 0 || T < 0 || n_streams > (int64_t)INT_MAX) return SDM_ECOUNT;
+    if (n_streams == 0 || T == 0) return SDM_OK;
+    if (!bank || !k_idx || !k_val || !v || !beta || !g || !q_idx || !q_val || !out) return SDM_ENULL;
+    const size_t es = bank_dtype == SDM_BF16 ? 2 : 4, is = idx_dtype == SDM_I64 ? 8 : 4;
+    if (!aligned(bank, es) || !aligned(out, es) || !aligned(k_idx, is) || !aligned(q_idx, is) || !aligned(k_val, 4) ||
+        !aligned(v, 4) || !aligned(beta, 4) || !aligned(g, 4) || !aligned(q_val, 4))
+        return SDM_EALIGN;
+    return SDM_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int sdm_decode_seq(void* bank, const void* k_idx, const float* k_val, const float* v, const float* beta,
+                   const float* g, const void* q_idx, const float* q_val, void* out, int64_t n_streams, int hd,
+                   int W, int R, int G, int T, int bank_dtype, int idx_dtype, sdm_stream_t stream) {
+    const int rc = check_decode(bank, k_idx, k_val, v, beta, g, q_idx, q_val, out, n_streams, hd, W, R, G, T,
+                                bank_dtype, idx_dtype);
+    if (rc != SDM_OK || n_streams == 0 || T == 0) return rc;
+    sdm::DecodeArgs a{};
+    a.bank = bank;
+    a.k_idx = k_idx;
+    a.k_val = k_val;
+    a.v = v;
+    a.beta = beta;
+    a.g = g;
+    a.q_idx = q_idx;
+    a.q_val = q_val;
+    a.out = out;
+    a.n_streams = n_streams;
+    a.hd = hd;
+    a.W = W;
+    a.R = R;
+    a.G = G;
+    a.T = T;
+    return sdm::launch_decode(a, bank_dtype, idx_dtype, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int sdm_decode_step(void* bank, const void* k_idx, const float* k_val, const float* v, const float* beta,
+                    const float* g, const void* q_idx, const float* q_val, void* out, int64_t n_streams, int hd,
+                    int W, int R, int G, int bank_dtype, int idx_dtype, sdm_stream_t stream) {
+    return sdm_decode_seq(bank, k_idx, k_val, v, beta, g, q_idx, q_val, out, n_streams, hd, W, R, G, 1, bank_dtype,
+                          idx_dtype, stream);
+}
+
+int sdm_gather(const void* bank, int64_t n_slots, int hd, int bank_dtype, int n_ops, const void* const idx[2],
+               const void* const w[2], float* const out[2], const int width[2], int idx_dtype, int w_dtype,
+               void* stash, int64_t tokens, int chunk, int valid, const int32_t* chunk_valid, sdm_stream_t stream) {
+    if (bank_dtype != SDM_BF16 && bank_dtype != SDM_F32) return SDM_EDTYPE;
+    if (w_dtype != SDM_BF16 && w_dtype != SDM_F32) return SDM_EDTYPE;
+    if (idx_dtype != SDM_I32 && idx_dtype != SDM_I64) return SDM_EIDX;
+    if (hd < 1 || hd > 65536) return SDM_EHD;
+    if (n_ops != 1 && n_ops != 2) return SDM_ENOPS;
+    if (!idx || !w || !out || !width) return SDM_ENULL;
+    for (int o = 0; o < n_ops; ++o)
+        if (width[o] < 1 || width[o] > 256) return SDM_EWIDTH;
+    if (n_slots < 1 || n_slots > (int64_t)INT_MAX || tokens < 0 || tokens > (int64_t)INT_MAX) return SDM_ECOUNT;
+    if (chunk < 1 || tokens % chunk != 0) return SDM_ECHUNK;
+    if (chunk_valid == nullptr && (valid < 0 || valid > chunk)) return SDM_ECHUNK;
+    if (tokens == 0) return SDM_OK;
+    if (!bank) return SDM_ENULL;
+    for (int o = 0; o < n_ops; ++o)
+        if (!idx[o] || !w[o] || !out[o]) return SDM_ENULL;
+    const size_t es = bank_dtype == SDM_BF16 ? 2 : 4, is = idx_dtype == SDM_I64 ? 8 : 4,
+                 ws = w_dtype == SDM_BF16 ? 2 : 4;
+    if (!aligned(bank, es) || (stash && !aligned(stash, es)) || (chunk_valid && !aligned(chunk_valid, 4)))
+        return SDM_EALIGN;
+    for (int o = 0; o < n_ops; ++o)
+        if (!aligned(idx[o], is) || !aligned(w[o], ws) || !aligned(out[o], 4)) return SDM_EALIGN;
+    const size_t bank_bytes = (size_t)n_slots * hd * es;
+    for (int o = 0; o < n_ops; ++o)
+        if (overlaps(out[o], (size_t)tokens * hd * 4, bank, bank_bytes)) return SDM_EOVERLAP;
+    if (stash && overlaps(stash, (size_t)tokens * width[0] * hd * es, bank, bank_bytes)) return SDM_EOVERLAP;
+
+    sdm::GatherArgs a{};
+    a.bank = bank;
+    a.n_slots = n_slots;
+    a.hd = hd;
+    a.n_ops = n_ops;
+    for (int o = 0; o < n_ops; ++o) {
+        a.idx[o] = idx[o];
+        a.w[o] = w[o];
+        a.out[o] = out[o];
+        a.width[o] = width[o];
+    }
+    a.stash = stash;
+    a.tokens = tokens;
+    a.chunk = chunk;
+    a.valid = valid;
+    a.chunk_valid = chunk_valid;
+    return sdm::launch_gather(a, bank_dtype, idx_dtype, w_dtype, reinterpret_cast<cudaStream_t>(stream));
+}
+
+const char* sdm_status_string(int status) {
+    switch (status) {
+        case SDM_OK: return "ok";
+        case SDM_ENULL: return "a required pointer is NULL";
+        case SDM_EDTYPE: return "bank or weight dtype must be SDM_BF16 or SDM_F32";
+        case SDM_EIDX: return "index dtype must be SDM_I32 or SDM_I64";
+        case SDM_EHD: return "head_dim must be in 1..65536";
+        case SDM_EWIDTH: return "W, R and gather widths must be in 1..256";
+        case SDM_EGATES: return "G must be 1 or W";
+        case SDM_ECOUNT: return "a count is negative or too large for one launch, or n_slots is outside 1..2^31-1";
+        case SDM_ECHUNK: return "need chunk >= 1, tokens a multiple of chunk and 0 <= valid <= chunk";
+        case SDM_EALIGN: return "a pointer is not aligned to its element size";
+        case SDM_EOVERLAP: return "a gather output or the stash overlaps the bank";
+        case SDM_ENOPS: return "the gather takes one or two operands";
+        default: break;
+    }
+    if (status > 0) return cudaGetErrorString(static_cast<cudaError_t>(status));
+    return "unknown status";
+}
+
+int sdm_device_status(unsigned int* status, int clear) {
+    if (!status) return SDM_ENULL;
+    unsigned int a = 0, b = 0;
+    int e = sdm::decode_status(&a, clear != 0);
+    if (e == 0) e = sdm::gather_status(&b, clear != 0);
+    *status = a | b;
+    if (e != 0) (void)cudaGetLastError();
+    return e;
+}
+
+int sdm_version(void) { return 100; }
+
+}  // extern "C"

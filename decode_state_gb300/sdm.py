@@ -1,0 +1,225 @@
+"""Python binding of the SDM C ABI (``include/sdm.h``): argument marshalling only.
+
+Every operation runs in the CUDA library ``_build/libsdm.so``; these wrappers check shapes and
+dtypes of PyTorch CUDA tensors, pass raw device pointers and the current CUDA stream, and raise
+``SDMError`` on a non-zero status. There is no fallback: without the built library every call
+raises.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_build", "libsdm.so")
+
+SDM_BF16, SDM_F32 = 0, 1
+SDM_I32, SDM_I64 = 0, 1
+SDM_DEV_TIMEOUT, SDM_DEV_BAD_INDEX = 1, 2
+
+ENTRY_POINTS = ("sdm_decode_step", "sdm_decode_seq", "sdm_gather", "sdm_status_string", "sdm_device_status",
+                "sdm_version")
+
+_BANK_CODES = {torch.bfloat16: SDM_BF16, torch.float32: SDM_F32}
+_IDX_CODES = {torch.int32: SDM_I32, torch.int64: SDM_I64}
+
+_lock = threading.Lock()
+_lib = None
+
+
+class SDMError(RuntimeError):
+    def __init__(self, fn: str, status: int, message: str):
+        super().__init__(f"{fn} failed with status {status}: {message}")
+        self.status = status
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def library() -> ctypes.CDLL:
+    """The loaded CUDA library; raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(_LIB_PATH):
+                raise RuntimeError(f"the SDM CUDA library is not built ({_LIB_PATH} is missing); "
+                                   "run decode_state_gb300.build.build()")
+            lib = ctypes.CDLL(_LIB_PATH)
+            vp, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+            dec = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i64, i32, i32, i32, i32]
+            lib.sdm_decode_step.argtypes = dec + [i32, i32, vp]
+            lib.sdm_decode_step.restype = i32
+            lib.sdm_decode_seq.argtypes = dec + [i32, i32, i32, vp]
+            lib.sdm_decode_seq.restype = i32
+            lib.sdm_gather.argtypes = [vp, i64, i32, i32, i32, ctypes.POINTER(vp), ctypes.POINTER(vp),
+                                       ctypes.POINTER(vp), ctypes.POINTER(i32), i32, i32, vp, i64, i32, i32, vp, vp]
+            lib.sdm_gather.restype = i32
+            lib.sdm_status_string.argtypes = [i32]
+            lib.sdm_status_string.restype = ctypes.c_char_p
+            lib.sdm_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint), i32]
+            lib.sdm_device_status.restype = i32
+            lib.sdm_version.argtypes = []
+            lib.sdm_version.restype = i32
+            _lib = lib
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return library().sdm_status_string(int(status)).decode()
+
+
+def _check(fn: str, status: int):
+    if status != 0:
+        raise SDMError(fn, status, status_string(status))
+
+
+def _stream_handle(stream, device) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _need(t: torch.Tensor, name: str, device):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda or t.device != device:
+        raise ValueError(f"{name} must be a CUDA tensor on {device}, got {t.device}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _shape(t: torch.Tensor, name: str, shape: tuple):
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+
+
+def _f32(t: torch.Tensor, name: str):
+    if t.dtype != torch.float32:
+        raise TypeError(f"{name} must be float32, got {t.dtype}")
+
+
+def _decode_args(bank, k_idx, k_val, v, beta, g, q_idx, q_val, out, lead: tuple, stream):
+    if bank.dtype not in _BANK_CODES:
+        raise TypeError(f"bank must be bfloat16 or float32, got {bank.dtype}")
+    if bank.dim() != 2:
+        raise ValueError("bank must be [n_slots, head_dim]")
+    dev = bank.device
+    if k_idx.dtype not in _IDX_CODES or q_idx.dtype != k_idx.dtype:
+        raise TypeError(f"k_idx and q_idx must share one dtype, int32 or int64; got {k_idx.dtype}, {q_idx.dtype}")
+    hd = bank.shape[1]
+    W, R, G = k_idx.shape[-1], q_idx.shape[-1], g.shape[-1]
+    for name, t, shp in (("k_idx", k_idx, (*lead, W)), ("k_val", k_val, (*lead, W)), ("v", v, (*lead, hd)),
+                         ("beta", beta, lead), ("g", g, (*lead, G)), ("q_idx", q_idx, (*lead, R)),
+                         ("q_val", q_val, (*lead, R))):
+        _need(t, name, dev)
+        _shape(t, name, shp)
+    for name, t in (("k_val", k_val), ("v", v), ("beta", beta), ("g", g), ("q_val", q_val)):
+        _f32(t, name)
+    _need(bank, "bank", dev)
+    if out is None:
+        out = torch.empty((*lead, hd), dtype=bank.dtype, device=dev)
+    _need(out, "out", dev)
+    _shape(out, "out", (*lead, hd))
+    if out.dtype != bank.dtype:
+        raise TypeError("out must have the bank dtype")
+    return out, (bank.data_ptr(), k_idx.data_ptr(), k_val.data_ptr(), v.data_ptr(), beta.data_ptr(), g.data_ptr(),
+                 q_idx.data_ptr(), q_val.data_ptr(), out.data_ptr()), hd, W, R, G, _stream_handle(stream, dev)
+
+
+def decode_step(bank, k_idx, k_val, v, beta, g, q_idx, q_val, out=None, stream=None) -> torch.Tensor:
+    """One write-then-read token for every stream (sdm_decode_step). Per-stream arrays are [S, .],
+    beta is [S]; the bank is updated in place; returns the readings [S, hd] in the bank dtype."""
+    S = k_idx.shape[0]
+    out, ptrs, hd, W, R, G, st = _decode_args(bank, k_idx, k_val, v, beta, g, q_idx, q_val, out, (S,), stream)
+    rc = library().sdm_decode_step(*ptrs, S, hd, W, R, G, _BANK_CODES[bank.dtype], _IDX_CODES[k_idx.dtype], st)
+    _check("sdm_decode_step", rc)
+    return out
+
+
+def decode_seq(bank, k_idx, k_val, v, beta, g, q_idx, q_val, out=None, stream=None) -> torch.Tensor:
+    """T tokens for every stream in one launch (sdm_decode_seq). Arrays are time-major [T, S, .],
+    beta is [T, S]; returns the readings [T, S, hd]."""
+    T, S = k_idx.shape[0], k_idx.shape[1]
+    out, ptrs, hd, W, R, G, st = _decode_args(bank, k_idx, k_val, v, beta, g, q_idx, q_val, out, (T, S), stream)
+    rc = library().sdm_decode_seq(*ptrs, S, hd, W, R, G, T, _BANK_CODES[bank.dtype], _IDX_CODES[k_idx.dtype], st)
+    _check("sdm_decode_seq", rc)
+    return out
+
+
+def gather(bank, ops, *, chunk: int, valid: int | None = None, chunk_valid=None, stash=None, with_stash=True,
+           outs=None, stream=None):
+    """Token gather (sdm_gather) with one or two operands ``ops = [(idx, w), ...]``.
+
+    idx [tokens, width] int32/int64, w [tokens, width] bf16/float32. Returns (outs, stash):
+    outs is a list of [tokens, hd] float32 tensors; stash [tokens, width0, hd] in the bank dtype
+    (allocated when ``with_stash`` and not given), or None. ``valid`` is the scalar count
+    (default: chunk) unless ``chunk_valid`` [tokens / chunk] int32 gives one per chunk.
+    """
+    if bank.dtype not in _BANK_CODES or bank.dim() != 2:
+        raise TypeError("bank must be a [n_slots, head_dim] bfloat16 or float32 tensor")
+    dev = bank.device
+    _need(bank, "bank", dev)
+    if len(ops) not in (1, 2):
+        raise ValueError("gather takes one or two operands")
+    n_slots, hd = bank.shape
+    tokens = ops[0][0].shape[0]
+    idx_dt, w_dt = ops[0][0].dtype, ops[0][1].dtype
+    if idx_dt not in _IDX_CODES or w_dt not in _BANK_CODES:
+        raise TypeError("indices must be int32/int64 and weights bfloat16/float32")
+    for o, (idx, w) in enumerate(ops):
+        _need(idx, f"idx[{o}]", dev)
+        _need(w, f"w[{o}]", dev)
+        if idx.dtype != idx_dt or w.dtype != w_dt:
+            raise TypeError("both operands must share the index dtype and the weight dtype")
+        if idx.dim() != 2 or idx.shape[0] != tokens or tuple(w.shape) != tuple(idx.shape):
+            raise ValueError(f"operand {o}: idx and w must both be [tokens, width]")
+    if outs is None:
+        outs = [torch.empty((tokens, hd), dtype=torch.float32, device=dev) for _ in ops]
+    for o, out in enumerate(outs):
+        _need(out, f"out[{o}]", dev)
+        _f32(out, f"out[{o}]")
+        _shape(out, f"out[{o}]", (tokens, hd))
+    if stash is None and with_stash:
+        stash = torch.empty((tokens, ops[0][0].shape[1], hd), dtype=bank.dtype, device=dev)
+    if stash is not None:
+        _need(stash, "stash", dev)
+        _shape(stash, "stash", (tokens, ops[0][0].shape[1], hd))
+        if stash.dtype != bank.dtype:
+            raise TypeError("stash must have the bank dtype")
+    if chunk_valid is not None:
+        _need(chunk_valid, "chunk_valid", dev)
+        if chunk_valid.dtype != torch.int32:
+            raise TypeError("chunk_valid must be int32")
+        if tokens % chunk == 0:
+            _shape(chunk_valid, "chunk_valid", (tokens // chunk,))
+    if valid is None:
+        valid = chunk
+    vp = ctypes.c_void_p
+    n = len(ops)
+    idx_arr = (vp * 2)(*[vp(op[0].data_ptr()) for op in ops], *([vp(0)] * (2 - n)))
+    w_arr = (vp * 2)(*[vp(op[1].data_ptr()) for op in ops], *([vp(0)] * (2 - n)))
+    out_arr = (vp * 2)(*[vp(o.data_ptr()) for o in outs], *([vp(0)] * (2 - n)))
+    width_arr = (ctypes.c_int * 2)(*[op[0].shape[1] for op in ops], *([0] * (2 - n)))
+    rc = library().sdm_gather(bank.data_ptr(), n_slots, hd, _BANK_CODES[bank.dtype], n, idx_arr, w_arr, out_arr,
+                              width_arr, _IDX_CODES[idx_dt], _BANK_CODES[w_dt],
+                              stash.data_ptr() if stash is not None else None, tokens, chunk, valid,
+                              chunk_valid.data_ptr() if chunk_valid is not None else None,
+                              _stream_handle(stream, dev))
+    _check("sdm_gather", rc)
+    return outs, stash
+
+
+def device_status(clear: bool = True) -> int:
+    """OR of the SDM_DEV_* bits kernels raised on the current device since the last clear."""
+    word = ctypes.c_uint(0)
+    rc = library().sdm_device_status(ctypes.byref(word), 1 if clear else 0)
+    _check("sdm_device_status", rc)
+    return int(word.value)
+
+
+def version() -> int:
+    return int(library().sdm_version())

@@ -1,0 +1,152 @@
+/*
+ * sdm.h - C ABI of the GB300 (sm_103a) sparse delta-memory (SDM) decode-state library.
+ *
+ * Three operations, each one kernel launch on the caller's stream:
+ *   sdm_decode_step  one write-then-read token for every stream
+ *   sdm_decode_seq   T tokens for every stream in one persistent launch
+ *   sdm_gather       per-token weighted sums of bank rows (one or two operands), optional stash
+ *
+ * Common rules
+ *   - Every pointer argument except `stream` is a DEVICE pointer the caller owns; the library
+ *     keeps no pointer after the call returns (apart from the work it enqueued) and frees nothing.
+ *   - Calls allocate no memory, synchronise nothing and only enqueue work on `stream` (NULL = the
+ *     legacy default stream), so they may be captured in a CUDA graph.
+ *   - Return value: 0 = launched (or nothing to do); < 0 = argument error (an SDM_E* code below,
+ *     nothing launched); > 0 = the cudaError_t of a failed launch (the error state is consumed).
+ *   - Index ranges are the caller's contract: decode slots must lie in the bank, every stream's
+ *     slots must be private to it and its W write slots distinct (none of this is checked, as in
+ *     the reference). The gather knows the bank's row count and skips out-of-range rows, raising
+ *     SDM_DEV_BAD_INDEX in the device status word (sdm_device_status).
+ *   - bfloat16 data is raw 16-bit patterns (the high half of an IEEE float32).
+ *   - Results are deterministic: every sum is accumulated in a fixed order independent of the GPU.
+ *
+ * Reference: the "sparse-delta-memory 2.0.0" wheel, files sparse_delta_memory/decode.py
+ * (sdm_decode_step, _decode_launch, _sdm_decode_kernel) and sparse_delta_memory/cuda/gather_cuda.py
+ * (module docstring, token_gather).
+ */
+#ifndef SDM_H
+#define SDM_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A CUDA stream handle; layout-compatible with cudaStream_t / CUstream. */
+typedef struct CUstream_st* sdm_stream_t;
+
+/* bank / weight element types */
+#define SDM_BF16 0
+#define SDM_F32 1
+/* index element types */
+#define SDM_I32 0
+#define SDM_I64 1
+
+/* argument errors (negative return values; nothing was launched) */
+#define SDM_OK 0
+#define SDM_ENULL (-1)      /* a required pointer is NULL */
+#define SDM_EDTYPE (-2)     /* bank or weight dtype is not SDM_BF16 / SDM_F32 */
+#define SDM_EIDX (-3)       /* index dtype is not SDM_I32 / SDM_I64 */
+#define SDM_EHD (-4)        /* head_dim < 1 or > 65536 */
+#define SDM_EWIDTH (-5)     /* W, R or a gather width outside 1..256 */
+#define SDM_EGATES (-6)     /* G is neither 1 nor W */
+#define SDM_ECOUNT (-7)     /* negative count, n_slots < 1 or >= 2^31, or more units than one launch holds */
+#define SDM_ECHUNK (-8)     /* chunk < 1, tokens not a multiple of chunk, or valid outside 0..chunk */
+#define SDM_EALIGN (-9)     /* a pointer is not aligned to its element size */
+#define SDM_EOVERLAP (-10)  /* a gather output or the stash overlaps the bank */
+#define SDM_ENOPS (-11)     /* gather operand count is not 1 or 2 */
+
+/* bits of the device status word */
+#define SDM_DEV_TIMEOUT 1u   /* a kernel gave up waiting for its own row copies (never expected) */
+#define SDM_DEV_BAD_INDEX 2u /* the gather met a row index outside [0, n_slots) and skipped it */
+
+/*
+ * sdm_decode_step - advance every stream by one token: write, then read.
+ *
+ * Defined by sdm_decode_step (decode.py): per stream s, with d_w = exp(g[s, G == 1 ? 0 : w]),
+ *     retrieved      = sum_w k_val[s,w] * d_w * bank[k_idx[s,w]]
+ *     delta_v        = beta[s] * (v[s] - retrieved)
+ *     bank[k_idx[w]] = d_w * bank[k_idx[w]] + k_val[s,w] * delta_v        (all w)
+ *     out[s]         = sum_r q_val[s,r] * bank[q_idx[s,r]]                (after the write)
+ * k_val, v and q_val are rounded to the bank dtype (round to nearest even) before use; beta and
+ * g are used in float32; d_w is the float32 nearest to e^g; all arithmetic is float32 and the
+ * new rows and the readings are rounded to the bank dtype.
+ *
+ *   bank      [n_slots, hd] bank dtype, row-major, updated in place
+ *   k_idx     [n_streams, W] idx dtype: write slots (distinct within a stream)
+ *   k_val     [n_streams, W] float32: write weights
+ *   v         [n_streams, hd] float32: values
+ *   beta      [n_streams] float32: write strengths
+ *   g         [n_streams, G] float32: log-decay per token (G == 1) or per write (G == W)
+ *   q_idx     [n_streams, R] idx dtype: read slots (repeats allowed)
+ *   q_val     [n_streams, R] float32: read weights
+ *   out       [n_streams, hd] bank dtype: readings
+ *   n_streams >= 0 (0: nothing launched); hd >= 1; 1 <= W, R <= 256; G in {1, W}
+ *   bank_dtype SDM_BF16 | SDM_F32; idx_dtype SDM_I32 | SDM_I64 (both index arrays)
+ */
+int sdm_decode_step(void* bank, const void* k_idx, const float* k_val, const float* v, const float* beta,
+                    const float* g, const void* q_idx, const float* q_val, void* out, int64_t n_streams, int hd,
+                    int W, int R, int G, int bank_dtype, int idx_dtype, sdm_stream_t stream);
+
+/*
+ * sdm_decode_seq - T tokens for every stream in one launch, equal to T sdm_decode_step calls.
+ *
+ * One block owns one (stream, column slice) for all T tokens; the reads of token t and the
+ * retrieve of token t+1 are ordered after token t's writes by a block barrier, which is valid
+ * because no other block touches those slots and columns (the barrier argument of
+ * _sdm_decode_kernel in decode.py).
+ *
+ * Every per-token array gains a leading time axis (time-major): k_idx, k_val [T, n_streams, W];
+ * v [T, n_streams, hd]; beta [T, n_streams]; g [T, n_streams, G]; q_idx, q_val [T, n_streams, R];
+ * out [T, n_streams, hd]. T >= 0 (0: nothing launched). Other arguments as sdm_decode_step.
+ */
+int sdm_decode_seq(void* bank, const void* k_idx, const float* k_val, const float* v, const float* beta,
+                   const float* g, const void* q_idx, const float* q_val, void* out, int64_t n_streams, int hd,
+                   int W, int R, int G, int T, int bank_dtype, int idx_dtype, sdm_stream_t stream);
+
+/*
+ * sdm_gather - token gather (gather_cuda.py, module docstring and token_gather).
+ *
+ * For every token t in [0, tokens) and operand o in [0, n_ops):
+ *     out[o][t, :] = sum_n w[o][t, n] * bank[idx[o][t, n], :]    (float32, ascending n, fmaf)
+ *     stash[t, n, :] = bank[idx[0][t, n], :]                      (raw rows of operand 0)
+ * Token t is padding when t % chunk >= valid_t, where valid_t = chunk_valid[t / chunk] if
+ * chunk_valid is not NULL, else `valid`. Padding tokens read nothing and get zero outputs and
+ * all-zero stash rows. The bank must not be written while the gather runs.
+ *
+ *   bank       [n_slots, hd] bank dtype (read only); 1 <= n_slots < 2^31
+ *   n_ops      1 or 2; idx[1], w[1], out[1], width[1] are ignored when n_ops == 1
+ *   idx[o]     [tokens, width[o]] idx dtype (same dtype for both operands)
+ *   w[o]       [tokens, width[o]] w dtype: SDM_BF16 or SDM_F32 (same for both operands)
+ *   out[o]     [tokens, hd] float32
+ *   width[o]   1..256
+ *   stash      [tokens, width[0], hd] bank dtype, or NULL for no stash
+ *   tokens     >= 0, a multiple of chunk; chunk >= 1; 0 <= valid <= chunk (ignored when
+ *              chunk_valid is given)
+ *   chunk_valid [tokens / chunk] int32 per-chunk valid counts in 0..chunk, or NULL
+ * The arrays idx, w, out and width are HOST arrays of two entries holding device pointers.
+ * Outputs and the stash must not overlap the bank.
+ */
+int sdm_gather(const void* bank, int64_t n_slots, int hd, int bank_dtype, int n_ops, const void* const idx[2],
+               const void* const w[2], float* const out[2], const int width[2], int idx_dtype, int w_dtype,
+               void* stash, int64_t tokens, int chunk, int valid, const int32_t* chunk_valid, sdm_stream_t stream);
+
+/* A static string naming a return code of the calls above. */
+const char* sdm_status_string(int status);
+
+/*
+ * sdm_device_status - read (and, if clear != 0, reset) the device status word of the current
+ * device: an OR of SDM_DEV_* bits raised by kernels since the last reset. Synchronises the
+ * device; not for use inside graph capture. Returns 0 or a cudaError_t; *status receives the word.
+ */
+int sdm_device_status(unsigned int* status, int clear);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int sdm_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SDM_H */

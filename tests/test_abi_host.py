@@ -1,0 +1,137 @@
+"""Host-side checks of the C ABI that need no GPU: the library builds and loads, exports every
+entry point include/sdm.h declares, and rejects bad arguments with the documented negative codes
+before touching CUDA. Every call here fails validation, so nothing is ever launched."""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+from decode_state_gb300 import build, sdm
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "sdm.h")
+
+
+def _codes():
+    text = open(HEADER).read()
+    return {m.group(1): int(m.group(2)) for m in re.finditer(r"#define (SDM_E\w+) \((-\d+)\)", text)}
+
+
+CODES = _codes()
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return sdm.library()
+
+
+def test_header_declares_the_entry_points():
+    text = open(HEADER).read()
+    declared = set(re.findall(r"^(?:int|const char\*) (sdm_\w+)\(", text, flags=re.M))
+    assert declared == set(sdm.ENTRY_POINTS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in sdm.ENTRY_POINTS:
+        assert hasattr(lib, name), name
+    assert sdm.version() == 100
+
+
+def test_status_strings(lib):
+    for name, code in CODES.items():
+        s = sdm.status_string(code)
+        assert s and s != "unknown status", name
+    assert sdm.status_string(0) == "ok"
+
+
+FAKE = 0x10000000  # never dereferenced: every call below fails validation first
+
+
+def _decode(lib, **kw):
+    a = dict(bank=FAKE, k_idx=FAKE, k_val=FAKE, v=FAKE, beta=FAKE, g=FAKE, q_idx=FAKE, q_val=FAKE, out=FAKE + 4096,
+             n_streams=4, hd=64, W=8, R=8, G=1, T=2, bank_dtype=0, idx_dtype=0)
+    a.update(kw)
+    return lib.sdm_decode_seq(a["bank"], a["k_idx"], a["k_val"], a["v"], a["beta"], a["g"], a["q_idx"], a["q_val"],
+                              a["out"], a["n_streams"], a["hd"], a["W"], a["R"], a["G"], a["T"], a["bank_dtype"],
+                              a["idx_dtype"], None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(bank_dtype=2), "SDM_EDTYPE"), (dict(idx_dtype=5), "SDM_EIDX"), (dict(hd=0), "SDM_EHD"),
+    (dict(hd=70000), "SDM_EHD"), (dict(W=0), "SDM_EWIDTH"), (dict(W=257), "SDM_EWIDTH"), (dict(R=0), "SDM_EWIDTH"),
+    (dict(R=300), "SDM_EWIDTH"), (dict(G=3), "SDM_EGATES"), (dict(W=4, G=8), "SDM_EGATES"),
+    (dict(n_streams=-1), "SDM_ECOUNT"), (dict(T=-2), "SDM_ECOUNT"), (dict(bank=0), "SDM_ENULL"),
+    (dict(q_val=0), "SDM_ENULL"), (dict(out=0), "SDM_ENULL"), (dict(bank=FAKE + 1), "SDM_EALIGN"),
+    (dict(bank=FAKE + 2, bank_dtype=1), "SDM_EALIGN"), (dict(k_idx=FAKE + 4, idx_dtype=1), "SDM_EALIGN"),
+    (dict(v=FAKE + 2), "SDM_EALIGN"),
+])
+def test_decode_argument_errors(lib, kw, code):
+    assert _decode(lib, **kw) == CODES[code]
+
+
+def test_decode_step_validates_like_seq(lib):
+    assert lib.sdm_decode_step(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4, 64, 0, 8, 1, 0, 0,
+                               None) == CODES["SDM_EWIDTH"]
+
+
+def test_decode_empty_is_ok_without_pointers(lib):
+    assert _decode(lib, n_streams=0, bank=0, out=0) == 0
+    assert _decode(lib, T=0, bank=0, out=0) == 0
+
+
+def _gather(lib, **kw):
+    a = dict(bank=FAKE, n_slots=1000, hd=64, bank_dtype=0, n_ops=2, idx=(FAKE + (1 << 24), FAKE + (2 << 24)),
+             w=(FAKE + (3 << 24), FAKE + (4 << 24)), out=(FAKE + (5 << 24), FAKE + (6 << 24)), width=(8, 4),
+             idx_dtype=1, w_dtype=0, stash=FAKE + (8 << 24), tokens=64, chunk=16, valid=16, chunk_valid=None)
+    a.update(kw)
+    vp = ctypes.c_void_p
+    idx = (vp * 2)(*a["idx"])
+    w = (vp * 2)(*a["w"])
+    out = (vp * 2)(*a["out"])
+    width = (ctypes.c_int * 2)(*a["width"])
+    return lib.sdm_gather(a["bank"], a["n_slots"], a["hd"], a["bank_dtype"], a["n_ops"], idx, w, out, width,
+                          a["idx_dtype"], a["w_dtype"], a["stash"], a["tokens"], a["chunk"], a["valid"],
+                          a["chunk_valid"], None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(bank_dtype=7), "SDM_EDTYPE"), (dict(w_dtype=3), "SDM_EDTYPE"), (dict(idx_dtype=-1), "SDM_EIDX"),
+    (dict(hd=0), "SDM_EHD"), (dict(n_ops=0), "SDM_ENOPS"), (dict(n_ops=3), "SDM_ENOPS"),
+    (dict(width=(0, 4)), "SDM_EWIDTH"), (dict(width=(8, 257)), "SDM_EWIDTH"), (dict(n_slots=0), "SDM_ECOUNT"),
+    (dict(n_slots=1 << 31), "SDM_ECOUNT"), (dict(tokens=-16), "SDM_ECOUNT"), (dict(chunk=0), "SDM_ECHUNK"),
+    (dict(tokens=60), "SDM_ECHUNK"), (dict(valid=17), "SDM_ECHUNK"), (dict(valid=-1), "SDM_ECHUNK"),
+    (dict(bank=0), "SDM_ENULL"), (dict(idx=(0, FAKE)), "SDM_ENULL"), (dict(out=(FAKE, 0)), "SDM_ENULL"),
+    (dict(bank=FAKE + 1), "SDM_EALIGN"), (dict(stash=FAKE + 1), "SDM_EALIGN"),
+    (dict(idx=(FAKE + 4, FAKE), idx_dtype=1), "SDM_EALIGN"), (dict(w=(FAKE + 1, FAKE)), "SDM_EALIGN"),
+    (dict(out=(FAKE + 64, FAKE + (6 << 24))), "SDM_EOVERLAP"), (dict(stash=FAKE + 128), "SDM_EOVERLAP"),
+])
+def test_gather_argument_errors(lib, kw, code):
+    assert _gather(lib, **kw) == CODES[code]
+
+
+def test_gather_second_operand_ignored_for_one_op(lib):
+    # with one operand, a NULL second operand is fine: the failure comes from the bad chunk
+    assert _gather(lib, n_ops=1, idx=(FAKE, 0), w=(FAKE, 0), out=(FAKE + (5 << 24), 0), chunk=0) == CODES["SDM_ECHUNK"]
+
+
+def test_gather_empty_is_ok(lib):
+    assert _gather(lib, tokens=0, bank=0) == 0
+
+
+def test_binding_rejects_host_tensors():
+    bank = torch.zeros((16, 8))
+    k = torch.zeros((2, 3), dtype=torch.int32)
+    f = torch.zeros((2, 3))
+    with pytest.raises(ValueError):
+        sdm.decode_step(bank, k, f, torch.zeros((2, 8)), torch.zeros(2), torch.zeros((2, 1)), k, f)
+
+
+def test_binding_rejects_bad_dtypes():
+    with pytest.raises(TypeError):
+        sdm.decode_step(torch.zeros((4, 4), dtype=torch.float16), *([torch.zeros(1)] * 7))

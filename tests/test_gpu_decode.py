@@ -1,0 +1,179 @@
+"""GPU parity of sdm_decode_step / sdm_decode_seq against the CPU oracle, through the C ABI.
+
+Small cases compare every reading and every bank element with the oracle; the full-size
+workloads run in the launch configuration the benchmark times and compare sampled streams (each
+stream owns a private slice of the bank, so the oracle can run a stream on its own).
+Tolerances are in parity.py: 1e-5*(1+|ref|) for float32, 2 bf16 ulps for bfloat16.
+"""
+
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from decode_state_gb300 import sdm, workloads
+from parity import DECODE_KEYS, assert_close, bits_equal, stream_slice, to_np
+
+pytestmark = pytest.mark.gpu
+
+DEV = torch.device("cuda:0") if torch.cuda.is_available() else None
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from decode_state_gb300 import build
+
+    build.build()
+    sdm.device_status(clear=True)
+    yield
+    assert sdm.device_status(clear=True) == 0, "a kernel raised the device status word"
+
+
+def _wl(dtype, idx, S, P, hd, W, R, G, T, seed=0):
+    return workloads.DecodeWorkload(f"t_{dtype}_{S}x{hd}_w{W}r{R}", dtype, S, hd, P, W, R, W if G == "W" else G, T,
+                                    idx, 0.35, bank_std=0.5, seed=seed)
+
+
+# (dtype, idx, streams, slots/stream, head_dim, W, R, G, T)
+SMALL = [
+    ("f32", "i32", 4, 1024, 64, 8, 8, 1, 16),       # the float32 decode workload's shape
+    ("bf16", "i64", 5, 300, 200, 16, 12, "W", 3),   # several column slices, ragged last slice, per-write gates
+    ("f32", "i64", 3, 700, 37, 5, 9, 1, 4),         # 148-byte rows: plain-load path
+    ("bf16", "i32", 2, 600, 13, 3, 256, "W", 2),    # odd bf16 rows, R at its maximum
+    ("f32", "i32", 7, 520, 256, 256, 256, 1, 2),    # W = R = 256, 1 KiB rows cut into slices
+    ("bf16", "i32", 33, 128, 128, 64, 64, 1, 5),    # the serving shape, fewer streams
+    ("bf16", "i64", 1, 64, 8, 1, 1, 1, 3),          # W = R = 1, 16-byte rows
+    ("f32", "i32", 2, 16, 1, 4, 4, "W", 3),         # head_dim 1
+]
+IDS = [f"{c[0]}-{c[1]}-S{c[2]}-hd{c[4]}-W{c[5]}R{c[6]}G{c[7]}-T{c[8]}" for c in SMALL]
+
+
+def _oracle_seq(x: dict):
+    bank = to_np(x["bank"])
+    out = oracle.decode_seq(bank, *(to_np(x[k]) for k in DECODE_KEYS))
+    return bank, out
+
+
+@pytest.mark.parametrize("case", SMALL, ids=IDS)
+def test_decode_seq_matches_oracle(case):
+    wl = _wl(*case)
+    x = workloads.make_decode_inputs(wl, device=DEV)
+    bank_ref, out_ref = _oracle_seq(x)
+    out = sdm.decode_seq(x["bank"], *(x[k] for k in DECODE_KEYS))
+    torch.cuda.synchronize()
+    assert_close(to_np(out), out_ref, wl.bank_dtype, "readings")
+    assert_close(to_np(x["bank"]), bank_ref, wl.bank_dtype, "bank")
+
+
+@pytest.mark.parametrize("case", SMALL, ids=IDS)
+def test_decode_step_matches_oracle(case):
+    wl = _wl(*case, seed=1)
+    x = workloads.make_decode_inputs(wl, device=DEV)
+    bank_ref, out_ref = _oracle_seq(x)
+    for t in range(wl.T):
+        out = sdm.decode_step(x["bank"], *(x[k][t] for k in DECODE_KEYS))
+        assert_close(to_np(out), out_ref[t], wl.bank_dtype, f"readings of token {t}")
+    assert_close(to_np(x["bank"]), bank_ref, wl.bank_dtype, "bank")
+
+
+@pytest.mark.parametrize("case", SMALL[:6], ids=IDS[:6])
+def test_seq_equals_steps_bitwise(case):
+    """One persistent launch of T tokens gives the same bits as T single-token launches."""
+    wl = _wl(*case, seed=2)
+    x = workloads.make_decode_inputs(wl, device=DEV)
+    bank2 = x["bank"].clone()
+    out_seq = sdm.decode_seq(x["bank"], *(x[k] for k in DECODE_KEYS))
+    outs = [sdm.decode_step(bank2, *(x[k][t] for k in DECODE_KEYS)) for t in range(wl.T)]
+    torch.cuda.synchronize()
+    assert torch.equal(out_seq.view(torch.int16 if wl.bank_dtype == "bf16" else torch.int32),
+                       torch.stack(outs).view(torch.int16 if wl.bank_dtype == "bf16" else torch.int32))
+    assert bits_equal(to_np(x["bank"]), to_np(bank2))
+
+
+def test_deterministic():
+    wl = _wl("bf16", "i32", 16, 256, 128, 32, 32, 1, 6, seed=3)
+    x = workloads.make_decode_inputs(wl, device=DEV)
+    bank0 = x["bank"].clone()
+    o1 = sdm.decode_seq(x["bank"], *(x[k] for k in DECODE_KEYS))
+    b1 = x["bank"].clone()
+    x["bank"].copy_(bank0)
+    o2 = sdm.decode_seq(x["bank"], *(x[k] for k in DECODE_KEYS))
+    torch.cuda.synchronize()
+    assert bits_equal(to_np(o1), to_np(o2)) and bits_equal(to_np(b1), to_np(x["bank"]))
+
+
+def test_empty_launches_are_noops():
+    wl = _wl("f32", "i32", 2, 16, 8, 2, 2, 1, 2)
+    x = workloads.make_decode_inputs(wl, device=DEV)
+    bank0 = x["bank"].clone()
+    sdm.decode_seq(x["bank"], *(x[k][:0] for k in DECODE_KEYS))  # T = 0
+    sdm.decode_step(x["bank"], *(x[k][0, :0] for k in DECODE_KEYS))  # no streams
+    torch.cuda.synchronize()
+    assert torch.equal(bank0, x["bank"])
+
+
+def test_read_slot_written_this_token():
+    """Readings of a slot written in the same token see the new row (read after write)."""
+    wl = _wl("bf16", "i64", 8, 64, 128, 4, 1, 1, 2, seed=4)
+    x = workloads.make_decode_inputs(wl, device=DEV)
+    x["q_idx"][:, :, 0] = x["k_idx"][:, :, 2]
+    x["q_val"][:] = 1.0
+    out = sdm.decode_seq(x["bank"], *(x[k] for k in DECODE_KEYS))
+    torch.cuda.synchronize()
+    last_rows = x["bank"][x["k_idx"][-1, :, 2].long()]
+    assert torch.equal(out[-1].view(torch.int16), last_rows.view(torch.int16))
+
+
+# ---------------------------------------------------------------- full-size workloads
+
+
+def _sampled_streams(S: int, n: int = 6):
+    return sorted(set([0, S - 1] + list(np.linspace(0, S - 1, n).astype(int))))
+
+
+def _oracle_stream(x: dict, s: int, P: int, bank_before: torch.Tensor):
+    """The oracle run of stream s alone, from that stream's bank rows before the GPU run.
+    Returns (readings [T, 1, hd], bank rows after)."""
+    xs = {k: x[k] for k in DECODE_KEYS}
+    xs["bank"] = x["bank"][:0]
+    ref_in = stream_slice(xs, s, P)
+    ref_in["bank"] = to_np(bank_before)
+    ref = oracle.decode_seq(ref_in["bank"], *(ref_in[k] for k in DECODE_KEYS))
+    return ref, ref_in["bank"]
+
+
+@pytest.mark.parametrize("wl", [workloads.C0, workloads.C2, workloads.C3], ids=lambda w: w.name)
+def test_full_size_seq(wl):
+    """The multi-token workloads as the benchmark launches them (one sdm_decode_seq call)."""
+    x = workloads.make_decode_inputs(wl, device=DEV)
+    P = wl.slots_per_stream
+    streams = _sampled_streams(wl.n_streams)
+    bank_before = {s: x["bank"][s * P:(s + 1) * P].clone() for s in streams}
+    out = sdm.decode_seq(x["bank"], *(x[k] for k in DECODE_KEYS))
+    torch.cuda.synchronize()
+    for s in streams:
+        ref, ref_bank = _oracle_stream(x, s, P, bank_before[s])
+        assert_close(to_np(out[:, s:s + 1]), ref, wl.bank_dtype, f"readings of stream {s}")
+        assert_close(to_np(x["bank"][s * P:(s + 1) * P]), ref_bank, wl.bank_dtype, f"slots of stream {s}")
+
+
+def test_full_size_steps_bf16_gw():
+    """The 256-step bf16 workload with per-write gates, as single-token launches; every step's
+    readings and the final bank of sampled streams against the oracle."""
+    wl = workloads.C1
+    x = workloads.make_decode_inputs(wl, device=DEV)
+    P = wl.slots_per_stream
+    streams = _sampled_streams(wl.n_streams)
+    bank_before = {s: x["bank"][s * P:(s + 1) * P].clone() for s in streams}
+    outs = torch.empty((wl.T, wl.n_streams, wl.hd), dtype=torch.bfloat16, device=DEV)
+    for t in range(wl.T):
+        sdm.decode_step(x["bank"], *(x[k][t] for k in DECODE_KEYS), out=outs[t])
+    torch.cuda.synchronize()
+    for s in streams:
+        ref, ref_bank = _oracle_stream(x, s, P, bank_before[s])
+        got = to_np(outs[:, s:s + 1])
+        for t0 in range(0, wl.T, 16):
+            assert_close(got[t0:t0 + 16], ref[t0:t0 + 16], "bf16", f"stream {s} tokens {t0}..{t0 + 15}")
+        assert_close(to_np(x["bank"][s * P:(s + 1) * P]), ref_bank, "bf16", f"slots of stream {s}")
