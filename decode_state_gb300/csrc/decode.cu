@@ -12,28 +12,32 @@
 // Design. One block owns one (stream, column slice) for every token it runs, so it is the only
 // writer and reader of those columns of the stream's private slots; a block barrier therefore
 // orders a token's writes before its reads and before the next token's retrieve (the argument
-// the reference kernel makes for its CTA barrier). Per token:
-//   1. the slots, rounded weights and gates go to shared memory;
-//   2. warp 0 issues one bulk copy (cp.async.bulk, async proxy) per write row slice into shared
-//      memory, all W in flight at once, completion counted on an mbarrier;
-//   3. each thread owns CPT adjacent columns and runs the retrieve as one fmaf chain over
-//      ascending w, then delta, then the decay-and-write, storing the new row slices to global
-//      memory with plain stores;
-//   4. fence.proxy.async.global + barrier make those stores visible to the next bulk copies;
-//   5. warp 0 bulk-copies the R read rows, each thread reduces its columns over ascending r and
-//      stores the readings.
-// Rows whose length is not a multiple of 16 bytes (or an unaligned bank) take a plain-load path
-// with one column per thread; a thread then only ever touches its own column, so program order
-// alone orders its writes and reads.
+// the reference kernel makes for its CTA barrier).
 //
-// Arithmetic per element (float32, no other fusion):
-//   a_w = kv_w * d_w;  retrieved = fmaf(a_w, row_w, .) over w;  delta = beta * (round(v) - retrieved)
-//   new_w = fmaf(kv_w, delta, row_w * d_w);  readings = fmaf(qv_r, row_r, .) over r
+// Vector path (rows a multiple of 16 bytes), per token:
+//   1. warp 0 issues one bulk copy (cp.async.bulk, async proxy) per write row slice into shared
+//      memory, all in flight at once, completion counted on an mbarrier; meanwhile every thread
+//      issues cp.async copies of the NEXT token's slots and weights, and thread 0 computes the next
+//      token's shared gate;
+//   2. each thread owns two adjacent columns, held as a packed float32 pair, and runs the
+//      retrieve as one chain of paired fmas over ascending w, then delta, then the decay-and-write
+//      (paired multiply and fma, one paired round to the bank dtype, one store per row);
+//   3. fence.proxy.async.global + barrier, then warp 0 bulk-copies the R read rows and each thread
+//      reduces its columns over ascending r;
+//   4. the prefetched metadata of the next token is turned into row byte offsets and broadcast
+//      weight pairs in shared memory.
+// Rows that are not a multiple of 16 bytes (or unaligned pointers) take a plain-load path with
+// one column per thread; a thread then only ever touches its own column, so program order alone
+// orders its writes and reads.
+//
+// Arithmetic per element (float32; every paired op is two independent round-to-nearest ops):
+//   a_w = kv_w * d_w;  retrieved = fma(a_w, row_w, .) over w;  delta = beta * (round(v) - retrieved)
+//   new_w = fma(kv_w, delta, row_w * d_w);  readings = fma(qv_r, row_r, .) over r
 // with d_w the float32 nearest to e^g (computed in double precision and rounded once).
 #include <algorithm>
 #include <climits>
 
-#include "../../include/sdm.h"
+#include "sdm.h"
 #include "sdm_device.cuh"
 #include "sdm_internal.h"
 
@@ -47,67 +51,154 @@ constexpr size_t kRowsBudget = 32 * 1024;  // staged rows of one block; with the
 
 __host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-// Shared-memory layout of one block (host and device agree on it).
-struct SmemLayout {
-    size_t rows, k_slot, q_slot, kv, aw, dw, qv, bar, total;
-    __host__ __device__ SmemLayout(int W, int R, int slice_cols, int es) {
+// ---------------------------------------------------------------- packed float32 pairs
+
+__device__ __forceinline__ uint64_t f2(float lo, float hi) {
+    return ((uint64_t)__float_as_uint(hi) << 32) | (uint64_t)__float_as_uint(lo);
+}
+__device__ __forceinline__ float f2lo(uint64_t x) { return __uint_as_float((uint32_t)x); }
+__device__ __forceinline__ float f2hi(uint64_t x) { return __uint_as_float((uint32_t)(x >> 32)); }
+__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ uint64_t fmul2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+// two adjacent bank elements as one word, widened to / narrowed from a float32 pair
+template <typename E>
+struct Pair;
+template <>
+struct Pair<uint16_t> {
+    using T = uint32_t;
+    __device__ static __forceinline__ uint64_t widen(uint32_t u) {
+        return f2(__uint_as_float(u << 16), __uint_as_float(u & 0xffff0000u));
+    }
+    __device__ static __forceinline__ uint32_t narrow(uint64_t x) {  // round to nearest even, both lanes
+        __nv_bfloat162 h = __floats2bfloat162_rn(f2lo(x), f2hi(x));
+        return *reinterpret_cast<uint32_t*>(&h);
+    }
+};
+template <>
+struct Pair<float> {
+    using T = uint64_t;
+    __device__ static __forceinline__ uint64_t widen(uint64_t u) { return u; }
+    __device__ static __forceinline__ uint64_t narrow(uint64_t x) { return x; }
+};
+
+// ---------------------------------------------------------------- vector-path layout
+
+struct VecLayout {
+    size_t rows, raw_k, raw_kv, raw_g, raw_q, raw_qv, raw_beta, koff, qoff, aw2, kv2, dw2, qv2, beta, dnext, bar,
+        total;
+    __host__ __device__ VecLayout(int W, int R, int G, int sw, int es, int is) {
         const int maxwr = W > R ? W : R;
         rows = 0;
-        k_slot = align_up((size_t)maxwr * slice_cols * es, 16);
-        q_slot = k_slot + (size_t)W * 8;
-        kv = q_slot + (size_t)R * 8;
-        aw = kv + (size_t)W * 4;
-        dw = aw + (size_t)W * 4;
-        qv = dw + (size_t)W * 4;
-        bar = align_up(qv + (size_t)R * 4, 8);
+        raw_k = align_up((size_t)maxwr * sw * es, 16);
+        raw_kv = align_up(raw_k + (size_t)W * is, 16);
+        raw_g = align_up(raw_kv + (size_t)W * 4, 16);
+        raw_q = align_up(raw_g + (size_t)G * 4, 16);
+        raw_qv = align_up(raw_q + (size_t)R * is, 16);
+        raw_beta = align_up(raw_qv + (size_t)R * 4, 16);
+        koff = align_up(raw_beta + 4, 16);
+        qoff = koff + (size_t)W * 8;
+        aw2 = qoff + (size_t)R * 8;
+        kv2 = aw2 + (size_t)W * 8;
+        dw2 = kv2 + (size_t)W * 8;
+        qv2 = dw2 + (size_t)W * 8;
+        beta = qv2 + (size_t)R * 8;
+        dnext = beta + 4;
+        bar = align_up(dnext + 4, 8);
         total = bar + 8;
     }
 };
 
-// Warp 0: bulk-copy n row slices (row_bytes each, starting at column c0) into rows[i * sw].
+__device__ __forceinline__ void cp_async4(void* dst, const void* src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async8(void* dst, const void* src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+// Every thread: cp.async copies of token ts's slots, weights, gates and beta into the raw area.
+template <typename I>
+__device__ __forceinline__ void prefetch_meta(const DecodeArgs& a, int64_t ts, const VecLayout& L,
+                                              unsigned char* smem) {
+    const int tid = threadIdx.x, nt = blockDim.x, W = a.W, R = a.R, G = a.G;
+    I* rk = reinterpret_cast<I*>(smem + L.raw_k);
+    I* rq = reinterpret_cast<I*>(smem + L.raw_q);
+    float* rkv = reinterpret_cast<float*>(smem + L.raw_kv);
+    float* rg = reinterpret_cast<float*>(smem + L.raw_g);
+    float* rqv = reinterpret_cast<float*>(smem + L.raw_qv);
+    const I* k_idx = static_cast<const I*>(a.k_idx) + ts * W;
+    const I* q_idx = static_cast<const I*>(a.q_idx) + ts * R;
+    for (int i = tid; i < W; i += nt) {
+        if constexpr (sizeof(I) == 8)
+            cp_async8(rk + i, k_idx + i);
+        else
+            cp_async4(rk + i, k_idx + i);
+        cp_async4(rkv + i, a.k_val + ts * W + i);
+    }
+    for (int i = tid; i < G; i += nt) cp_async4(rg + i, a.g + ts * G + i);
+    for (int i = tid; i < R; i += nt) {
+        if constexpr (sizeof(I) == 8)
+            cp_async8(rq + i, q_idx + i);
+        else
+            cp_async4(rq + i, q_idx + i);
+        cp_async4(rqv + i, a.q_val + ts * R + i);
+    }
+    if (tid == 0) cp_async4(smem + L.raw_beta, a.beta + ts);
+    cp_async_commit();
+}
+
+// Every thread: turn the raw copies into row byte offsets and broadcast weight pairs.
+template <typename E, typename I>
+__device__ __forceinline__ void derive_meta(const DecodeArgs& a, int c0, const VecLayout& L, unsigned char* smem) {
+    const int tid = threadIdx.x, nt = blockDim.x, W = a.W, R = a.R, G = a.G;
+    const int64_t rowb = (int64_t)a.hd * sizeof(E), colb = (int64_t)c0 * sizeof(E);
+    const I* rk = reinterpret_cast<const I*>(smem + L.raw_k);
+    const I* rq = reinterpret_cast<const I*>(smem + L.raw_q);
+    const float* rkv = reinterpret_cast<const float*>(smem + L.raw_kv);
+    const float* rg = reinterpret_cast<const float*>(smem + L.raw_g);
+    const float* rqv = reinterpret_cast<const float*>(smem + L.raw_qv);
+    int64_t* koff = reinterpret_cast<int64_t*>(smem + L.koff);
+    int64_t* qoff = reinterpret_cast<int64_t*>(smem + L.qoff);
+    uint64_t* aw2 = reinterpret_cast<uint64_t*>(smem + L.aw2);
+    uint64_t* kv2 = reinterpret_cast<uint64_t*>(smem + L.kv2);
+    uint64_t* dw2 = reinterpret_cast<uint64_t*>(smem + L.dw2);
+    uint64_t* qv2 = reinterpret_cast<uint64_t*>(smem + L.qv2);
+    const float d1 = *reinterpret_cast<const float*>(smem + L.dnext);
+    for (int i = tid; i < W; i += nt) {
+        koff[i] = (int64_t)rk[i] * rowb + colb;
+        const float k = round_to<E>(rkv[i]);
+        const float d = G == 1 ? d1 : (float)exp((double)rg[i]);
+        const float aa = __fmul_rn(k, d);
+        kv2[i] = f2(k, k);
+        aw2[i] = f2(aa, aa);
+        dw2[i] = f2(d, d);
+    }
+    for (int i = tid; i < R; i += nt) {
+        qoff[i] = (int64_t)rq[i] * rowb + colb;
+        const float q = round_to<E>(rqv[i]);
+        qv2[i] = f2(q, q);
+    }
+    if (tid == 0) *reinterpret_cast<float*>(smem + L.beta) = *reinterpret_cast<const float*>(smem + L.raw_beta);
+}
+
+// Warp 0: bulk-copy n row slices (row_bytes each) at byte offsets off[] into rows[i * sw].
 template <typename E>
-__device__ __forceinline__ void issue_rows(E* rows, const E* bank, const int64_t* slot, int n, int hd, int c0,
-                                           int sw, uint32_t row_bytes, uint64_t* bar) {
+__device__ __forceinline__ void issue_rows_off(E* rows, const unsigned char* bank, const int64_t* off, int n, int sw,
+                                               uint32_t row_bytes, uint64_t* bar) {
     const int lane = threadIdx.x;
     if (lane == 0) mbar_arrive_expect_tx(bar, row_bytes * (uint32_t)n);
     __syncwarp();
-    for (int i = lane; i < n; i += 32) bulk_g2s(rows + (size_t)i * sw, bank + slot[i] * hd + c0, row_bytes, bar);
-}
-
-// Plain-load path: this thread's column of n rows into rows[i * sw + j].
-template <typename E>
-__device__ __forceinline__ void load_rows_simt(E* rows, const E* bank, const int64_t* slot, int n, int hd, int col,
-                                               int sw, int j) {
-    int i = 0;
-    for (; i + 8 <= n; i += 8) {
-        E x[8];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) x[u] = bank[slot[i + u] * hd + col];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) rows[(size_t)(i + u) * sw + j] = x[u];
-    }
-    for (; i < n; ++i) rows[(size_t)i * sw + j] = bank[slot[i] * hd + col];
-}
-
-// CPT adjacent elements of a staged row, widened to float32.
-template <typename E, int CPT>
-__device__ __forceinline__ void read_staged(const E* p, float (&x)[CPT]) {
-    if constexpr (CPT == 2) {
-        const uint32_t u = *reinterpret_cast<const uint32_t*>(p);
-        x[0] = __uint_as_float(u << 16);
-        x[1] = __uint_as_float(u & 0xffff0000u);
-    } else {
-        x[0] = to_f32(p[0]);
-    }
-}
-
-template <typename E, int CPT>
-__device__ __forceinline__ void store_elems(E* p, const float (&x)[CPT]) {
-    if constexpr (CPT == 2) {
-        *reinterpret_cast<uint32_t*>(p) = pack_bf16x2(x[0], x[1]);
-    } else {
-        p[0] = from_f32<E>(x[0]);
-    }
+    for (int i = lane; i < n; i += 32) bulk_g2s(rows + (size_t)i * sw, bank + off[i], row_bytes, bar);
 }
 
 // Wait for the current bulk phase; on a timeout every thread of the block learns it at the
@@ -126,15 +217,163 @@ __device__ __forceinline__ bool wait_phase(uint64_t* bar, uint32_t& parity, int*
     return true;
 }
 
-template <typename E, typename I, bool BULK>
-__global__ void __launch_bounds__(kMaxThreads) decode_kernel(const DecodeArgs a) {
+template <typename E, typename I>
+__global__ void __launch_bounds__(kMaxThreads, 2) decode_vec_kernel(const DecodeArgs a) {
+    using P = Pair<E>;
+    using PT = typename P::T;
     constexpr int ES = sizeof(E);
-    constexpr int CPT = (BULK && ES == 2) ? 2 : 1;
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ int s_abort;
 
     const int W = a.W, R = a.R, G = a.G, hd = a.hd, sw = a.slice_cols;
-    const SmemLayout L(W, R, sw, ES);
+    const VecLayout L(W, R, G, sw, ES, (int)sizeof(I));
+    E* rows = reinterpret_cast<E*>(smem + L.rows);
+    const int64_t* koff = reinterpret_cast<const int64_t*>(smem + L.koff);
+    const int64_t* qoff = reinterpret_cast<const int64_t*>(smem + L.qoff);
+    const uint64_t* aw2 = reinterpret_cast<const uint64_t*>(smem + L.aw2);
+    const uint64_t* kv2 = reinterpret_cast<const uint64_t*>(smem + L.kv2);
+    const uint64_t* dw2 = reinterpret_cast<const uint64_t*>(smem + L.dw2);
+    const uint64_t* qv2 = reinterpret_cast<const uint64_t*>(smem + L.qv2);
+    uint64_t* bar = reinterpret_cast<uint64_t*>(smem + L.bar);
+
+    const int tid = threadIdx.x;
+    const int64_t s = blockIdx.x / a.n_slices;
+    const int c0 = (int)(blockIdx.x % a.n_slices) * sw;
+    const int ncols = min(sw, hd - c0);
+    const int j = 2 * tid;  // this thread's first column within the slice
+    const bool active = j < ncols;
+    const uint32_t row_bytes = (uint32_t)ncols * ES;
+    const int pstride = sw / 2;  // pairs per staged row
+    unsigned char* bank = static_cast<unsigned char*>(a.bank);
+    E* out = static_cast<E*>(a.out);
+    const PT* rp = reinterpret_cast<const PT*>(rows) + tid;
+    const int64_t jb = (int64_t)j * ES;
+
+    if (tid == 0) {
+        s_abort = 0;
+        mbar_init(bar, 1);
+        mbar_init_fence();
+    }
+    prefetch_meta<I>(a, s, L, smem);  // token 0
+    cp_async_wait_all();
+    __syncthreads();
+    if (G == 1 && tid == 0)
+        *reinterpret_cast<float*>(smem + L.dnext) = (float)exp((double)*reinterpret_cast<const float*>(smem + L.raw_g));
+    __syncthreads();
+    derive_meta<E, I>(a, c0, L, smem);
+    __syncthreads();
+    uint32_t parity = 0;
+
+    for (int t = 0; t < a.T; ++t) {
+        const int64_t ts = (int64_t)t * a.n_streams + s;  // (token, stream) row of the time-major inputs
+
+        // 1. the write rows; the next token's metadata meanwhile
+        if (tid < 32) issue_rows_off<E>(rows, bank, koff, W, sw, row_bytes, bar);
+        uint64_t vr = 0;
+        if (active) {
+            const float2 vv = __ldg(reinterpret_cast<const float2*>(a.v + ts * hd + c0 + j));
+            vr = P::widen(P::narrow(f2(vv.x, vv.y)));  // rounded to the bank dtype
+        }
+        const float beta = *reinterpret_cast<const float*>(smem + L.beta);
+        const uint64_t dsh = dw2[0];
+        if (t + 1 < a.T) {
+            prefetch_meta<I>(a, ts + a.n_streams, L, smem);
+            if (G == 1 && tid == 0)  // the next token's shared gate, while this token's rows are in flight
+                *reinterpret_cast<float*>(smem + L.dnext) = (float)exp((double)__ldg(a.g + ts + a.n_streams));
+        }
+        if (!wait_phase(bar, parity, &s_abort)) return;
+
+        // 2. retrieve, delta, decay-and-write
+        if (active) {
+            uint64_t acc = 0;
+            int w = 0;
+            for (; w + 4 <= W; w += 4) {
+                const PT x0 = rp[(w + 0) * pstride], x1 = rp[(w + 1) * pstride];
+                const PT x2 = rp[(w + 2) * pstride], x3 = rp[(w + 3) * pstride];
+                acc = ffma2(aw2[w + 0], P::widen(x0), acc);
+                acc = ffma2(aw2[w + 1], P::widen(x1), acc);
+                acc = ffma2(aw2[w + 2], P::widen(x2), acc);
+                acc = ffma2(aw2[w + 3], P::widen(x3), acc);
+            }
+            for (; w < W; ++w) acc = ffma2(aw2[w], P::widen(rp[w * pstride]), acc);
+            const float dl = __fmul_rn(beta, __fsub_rn(f2lo(vr), f2lo(acc)));
+            const float dh = __fmul_rn(beta, __fsub_rn(f2hi(vr), f2hi(acc)));
+            const uint64_t delta = f2(dl, dh);
+#pragma unroll 4
+            for (w = 0; w < W; ++w) {
+                const uint64_t x = P::widen(rp[w * pstride]);
+                const uint64_t y = ffma2(kv2[w], delta, fmul2(x, G == 1 ? dsh : dw2[w]));
+                *reinterpret_cast<PT*>(bank + koff[w] + jb) = P::narrow(y);
+            }
+        }
+        fence_proxy_async_global();
+        __syncthreads();
+
+        // 3. the read rows, after the write
+        if (tid < 32) issue_rows_off<E>(rows, bank, qoff, R, sw, row_bytes, bar);
+        if (!wait_phase(bar, parity, &s_abort)) return;
+        if (active) {
+            uint64_t acc = 0;
+            int r = 0;
+            for (; r + 4 <= R; r += 4) {
+                const PT x0 = rp[(r + 0) * pstride], x1 = rp[(r + 1) * pstride];
+                const PT x2 = rp[(r + 2) * pstride], x3 = rp[(r + 3) * pstride];
+                acc = ffma2(qv2[r + 0], P::widen(x0), acc);
+                acc = ffma2(qv2[r + 1], P::widen(x1), acc);
+                acc = ffma2(qv2[r + 2], P::widen(x2), acc);
+                acc = ffma2(qv2[r + 3], P::widen(x3), acc);
+            }
+            for (; r < R; ++r) acc = ffma2(qv2[r], P::widen(rp[r * pstride]), acc);
+            *reinterpret_cast<PT*>(out + ts * hd + c0 + j) = P::narrow(acc);
+        }
+
+        // 4. the next token's metadata (rows and metadata of this token are no longer read)
+        cp_async_wait_all();
+        __syncthreads();
+        if (t + 1 < a.T) derive_meta<E, I>(a, c0, L, smem);
+        __syncthreads();
+    }
+}
+
+// ---------------------------------------------------------------- plain-load path
+
+struct SimtLayout {
+    size_t rows, k_slot, q_slot, kv, aw, dw, qv, total;
+    __host__ __device__ SimtLayout(int W, int R, int slice_cols, int es) {
+        const int maxwr = W > R ? W : R;
+        rows = 0;
+        k_slot = align_up((size_t)maxwr * slice_cols * es, 16);
+        q_slot = k_slot + (size_t)W * 8;
+        kv = q_slot + (size_t)R * 8;
+        aw = kv + (size_t)W * 4;
+        dw = aw + (size_t)W * 4;
+        qv = dw + (size_t)W * 4;
+        total = qv + (size_t)R * 4;
+    }
+};
+
+// This thread's column of n rows into rows[i * sw + j].
+template <typename E>
+__device__ __forceinline__ void load_rows_simt(E* rows, const E* bank, const int64_t* slot, int n, int hd, int col,
+                                               int sw, int j) {
+    int i = 0;
+    for (; i + 8 <= n; i += 8) {
+        E x[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) x[u] = bank[slot[i + u] * hd + col];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) rows[(size_t)(i + u) * sw + j] = x[u];
+    }
+    for (; i < n; ++i) rows[(size_t)i * sw + j] = bank[slot[i] * hd + col];
+}
+
+template <typename E, typename I>
+__global__ void __launch_bounds__(kMaxThreads) decode_simt_kernel(const DecodeArgs a) {
+    constexpr int ES = sizeof(E);
+    extern __shared__ __align__(128) unsigned char smem[];
+
+    const int W = a.W, R = a.R, G = a.G, hd = a.hd, sw = a.slice_cols;
+    const SimtLayout L(W, R, sw, ES);
     E* rows = reinterpret_cast<E*>(smem + L.rows);
     int64_t* k_slot = reinterpret_cast<int64_t*>(smem + L.k_slot);
     int64_t* q_slot = reinterpret_cast<int64_t*>(smem + L.q_slot);
@@ -142,32 +381,18 @@ __global__ void __launch_bounds__(kMaxThreads) decode_kernel(const DecodeArgs a)
     float* aw = reinterpret_cast<float*>(smem + L.aw);
     float* dw = reinterpret_cast<float*>(smem + L.dw);
     float* qv = reinterpret_cast<float*>(smem + L.qv);
-    uint64_t* bar = reinterpret_cast<uint64_t*>(smem + L.bar);
 
     const int tid = threadIdx.x, nt = blockDim.x;
     const int64_t s = blockIdx.x / a.n_slices;
     const int c0 = (int)(blockIdx.x % a.n_slices) * sw;
     const int ncols = min(sw, hd - c0);
-    const int j = tid * CPT;  // this thread's first column within the slice
+    const int j = tid;
     const bool active = j < ncols;
-    const uint32_t row_bytes = (uint32_t)ncols * ES;
     E* bank = static_cast<E*>(a.bank);
     E* out = static_cast<E*>(a.out);
 
-    if (tid == 0) {
-        s_abort = 0;
-        if (BULK) {
-            mbar_init(bar, 1);
-            mbar_init_fence();
-        }
-    }
-    __syncthreads();
-    uint32_t parity = 0;
-
     for (int t = 0; t < a.T; ++t) {
-        const int64_t ts = (int64_t)t * a.n_streams + s;  // (token, stream) row of the time-major inputs
-
-        // 1. per-token metadata
+        const int64_t ts = (int64_t)t * a.n_streams + s;
         for (int i = tid; i < W; i += nt) {
             const int64_t e = ts * W + i;
             k_slot[i] = load_index<I>(a.k_idx, e);
@@ -180,92 +405,48 @@ __global__ void __launch_bounds__(kMaxThreads) decode_kernel(const DecodeArgs a)
             q_slot[i] = load_index<I>(a.q_idx, e);
             qv[i] = round_to<E>(__ldg(a.q_val + e));
         }
-        float vr[CPT];
-#pragma unroll
-        for (int k = 0; k < CPT; ++k) vr[k] = active ? round_to<E>(__ldg(a.v + ts * hd + c0 + j + k)) : 0.0f;
+        const float vr = active ? round_to<E>(__ldg(a.v + ts * hd + c0 + j)) : 0.0f;
         const float beta = __ldg(a.beta + ts);
         __syncthreads();
-
-        // 2. the write rows
-        if (BULK) {
-            if (tid < 32) issue_rows<E>(rows, bank, k_slot, W, hd, c0, sw, row_bytes, bar);
-        } else if (active) {
-            load_rows_simt<E>(rows, bank, k_slot, W, hd, c0 + j, sw, j);
-        }
+        if (active) load_rows_simt<E>(rows, bank, k_slot, W, hd, c0 + j, sw, j);
         for (int i = tid; i < W; i += nt) aw[i] = __fmul_rn(kv[i], dw[G == 1 ? 0 : i]);
-        if (BULK) {
-            if (!wait_phase(bar, parity, &s_abort)) return;
-        } else {
-            __syncthreads();
-        }
-
-        // 3. retrieve, delta, decay-and-write for this thread's columns
-        if (active) {
-            float acc[CPT];
-#pragma unroll
-            for (int k = 0; k < CPT; ++k) acc[k] = 0.0f;
-            for (int w = 0; w < W; ++w) {
-                float x[CPT];
-                read_staged<E, CPT>(rows + (size_t)w * sw + j, x);
-                const float a_w = aw[w];
-#pragma unroll
-                for (int k = 0; k < CPT; ++k) acc[k] = fmaf(a_w, x[k], acc[k]);
-            }
-            float delta[CPT];
-#pragma unroll
-            for (int k = 0; k < CPT; ++k) delta[k] = __fmul_rn(beta, __fsub_rn(vr[k], acc[k]));
-            for (int w = 0; w < W; ++w) {
-                float x[CPT], y[CPT];
-                read_staged<E, CPT>(rows + (size_t)w * sw + j, x);
-                const float kvw = kv[w], dww = dw[G == 1 ? 0 : w];
-#pragma unroll
-                for (int k = 0; k < CPT; ++k) y[k] = fmaf(kvw, delta[k], __fmul_rn(x[k], dww));
-                store_elems<E, CPT>(bank + k_slot[w] * hd + c0 + j, y);
-            }
-        }
-        if (BULK) fence_proxy_async_global();
         __syncthreads();
-
-        // 4. the read rows, after the write
-        if (BULK) {
-            if (tid < 32) issue_rows<E>(rows, bank, q_slot, R, hd, c0, sw, row_bytes, bar);
-            if (!wait_phase(bar, parity, &s_abort)) return;
-        } else if (active) {
-            load_rows_simt<E>(rows, bank, q_slot, R, hd, c0 + j, sw, j);
-        }
-
-        // 5. readings
         if (active) {
-            float acc[CPT];
-#pragma unroll
-            for (int k = 0; k < CPT; ++k) acc[k] = 0.0f;
-            for (int r = 0; r < R; ++r) {
-                float x[CPT];
-                read_staged<E, CPT>(rows + (size_t)r * sw + j, x);
-                const float q = qv[r];
-#pragma unroll
-                for (int k = 0; k < CPT; ++k) acc[k] = fmaf(q, x[k], acc[k]);
+            float acc = 0.0f;
+            for (int w = 0; w < W; ++w) acc = fmaf(aw[w], to_f32(rows[(size_t)w * sw + j]), acc);
+            const float delta = __fmul_rn(beta, __fsub_rn(vr, acc));
+            for (int w = 0; w < W; ++w) {
+                const float x = to_f32(rows[(size_t)w * sw + j]);
+                bank[k_slot[w] * hd + c0 + j] = from_f32<E>(fmaf(kv[w], delta, __fmul_rn(x, dw[G == 1 ? 0 : w])));
             }
-            store_elems<E, CPT>(out + ts * hd + c0 + j, acc);
+            load_rows_simt<E>(rows, bank, q_slot, R, hd, c0 + j, sw, j);
+            acc = 0.0f;
+            for (int r = 0; r < R; ++r) acc = fmaf(qv[r], to_f32(rows[(size_t)r * sw + j]), acc);
+            out[ts * hd + c0 + j] = from_f32<E>(acc);
         }
-        __syncthreads();  // metadata and rows are rewritten by the next token
+        __syncthreads();  // metadata is rewritten by the next token
     }
 }
 
-template <typename E, typename I, bool BULK>
-int launch_typed(const DecodeArgs& a, dim3 grid, dim3 block, size_t smem, cudaStream_t stream) {
-    decode_kernel<E, I, BULK><<<grid, block, smem, stream>>>(a);
+// ---------------------------------------------------------------- launch
+
+template <typename K>
+int launch_kernel(K kernel, const DecodeArgs& a, dim3 grid, dim3 block, size_t smem, cudaStream_t stream) {
+    if (smem > 48 * 1024) {  // opt in to more than the default dynamic shared memory
+        const cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return (int)e;
+    }
+    kernel<<<grid, block, smem, stream>>>(a);
     return (int)cudaGetLastError();
 }
 
 template <typename E, typename I>
-int launch_bulk_or_simt(bool bulk, const DecodeArgs& a, dim3 grid, dim3 block, size_t smem, cudaStream_t stream) {
-    return bulk ? launch_typed<E, I, true>(a, grid, block, smem, stream)
-                : launch_typed<E, I, false>(a, grid, block, smem, stream);
+int launch_typed(bool vec, const DecodeArgs& a, dim3 grid, dim3 block, size_t smem, cudaStream_t stream) {
+    return vec ? launch_kernel(decode_vec_kernel<E, I>, a, grid, block, smem, stream)
+               : launch_kernel(decode_simt_kernel<E, I>, a, grid, block, smem, stream);
 }
 
-int shrink_cols(int sw, bool bulk, int es) {
-    const int q = bulk ? 16 / es : 32;
+int shrink_cols(int sw, int q) {
     const int half = (sw / 2 + q - 1) / q * q;
     return std::max(q, half);
 }
@@ -276,18 +457,22 @@ int launch_decode(const DecodeArgs& a0, int bank_dtype, int idx_dtype, cudaStrea
     DecodeArgs a = a0;
     if (a.n_streams == 0 || a.T == 0) return 0;
     const int es = bank_dtype == SDM_BF16 ? 2 : 4;
-    const bool bulk = ((int64_t)a.hd * es) % 16 == 0 && reinterpret_cast<uintptr_t>(a.bank) % 16 == 0;
-    const int cpt = (bulk && es == 2) ? 2 : 1;
+    const int is = idx_dtype == SDM_I64 ? 8 : 4;
+    const auto al = [](const void* p, uintptr_t n) { return reinterpret_cast<uintptr_t>(p) % n == 0; };
+    // vector path: whole 16-byte row chunks for the bulk copies, column pairs for the threads
+    const bool vec = ((int64_t)a.hd * es) % 16 == 0 && al(a.bank, 16) && al(a.out, 2 * es) && al(a.v, 8);
+    const int cpt = vec ? 2 : 1;
+    const int q = vec ? 16 / es : 32;  // slice granularity in columns
     const int maxwr = std::max(a.W, a.R);
 
     // Column slice: the whole row when it fits; narrower to bound shared memory and to give the
     // grid at least two blocks per SM when there are few streams.
     int sw = std::min(a.hd, kMaxThreads * cpt);
-    if (bulk) sw = sw / (16 / es) * (16 / es);
-    while ((size_t)maxwr * sw * es > kRowsBudget && sw > (bulk ? 16 / es : 32)) sw = shrink_cols(sw, bulk, es);
+    if (vec) sw = sw / q * q;
+    while ((size_t)maxwr * sw * es > kRowsBudget && sw > q) sw = shrink_cols(sw, q);
     const int64_t want_blocks = 2LL * sm_count();
     while (a.n_streams * ((a.hd + sw - 1) / sw) < want_blocks && sw * es > 128) {
-        const int next = shrink_cols(sw, bulk, es);
+        const int next = shrink_cols(sw, q);
         if (next >= sw) break;
         sw = next;
     }
@@ -296,15 +481,15 @@ int launch_decode(const DecodeArgs& a0, int bank_dtype, int idx_dtype, cudaStrea
     const int64_t blocks = a.n_streams * a.n_slices;
     if (blocks > INT_MAX) return SDM_ECOUNT;
     const int threads = ((sw + cpt - 1) / cpt + 31) / 32 * 32;
-    const size_t smem = SmemLayout(a.W, a.R, sw, es).total;
+    const size_t smem = vec ? VecLayout(a.W, a.R, a.G, sw, es, is).total : SimtLayout(a.W, a.R, sw, es).total;
 
     const dim3 grid((unsigned)blocks), block((unsigned)threads);
     if (bank_dtype == SDM_BF16) {
-        return idx_dtype == SDM_I32 ? launch_bulk_or_simt<uint16_t, int32_t>(bulk, a, grid, block, smem, stream)
-                                    : launch_bulk_or_simt<uint16_t, int64_t>(bulk, a, grid, block, smem, stream);
+        return idx_dtype == SDM_I32 ? launch_typed<uint16_t, int32_t>(vec, a, grid, block, smem, stream)
+                                    : launch_typed<uint16_t, int64_t>(vec, a, grid, block, smem, stream);
     }
-    return idx_dtype == SDM_I32 ? launch_bulk_or_simt<float, int32_t>(bulk, a, grid, block, smem, stream)
-                                : launch_bulk_or_simt<float, int64_t>(bulk, a, grid, block, smem, stream);
+    return idx_dtype == SDM_I32 ? launch_typed<float, int32_t>(vec, a, grid, block, smem, stream)
+                                : launch_typed<float, int64_t>(vec, a, grid, block, smem, stream);
 }
 
 int decode_status(unsigned int* word, bool clear) {

@@ -18,7 +18,7 @@
 #include <algorithm>
 #include <climits>
 
-#include "../../include/sdm.h"
+#include "sdm.h"
 #include "sdm_device.cuh"
 #include "sdm_internal.h"
 

@@ -4,7 +4,7 @@
 #include <atomic>
 #include <climits>
 
-#include "../../include/sdm.h"
+#include "sdm.h"
 #include "sdm_internal.h"
 
 namespace sdm {
