@@ -234,7 +234,7 @@ class Case:
             self.unit = UNIT
             self.launches = 1 if wl.mode == "seq" else wl.T
             self.nbytes = workloads.decode_bytes_per_stream_token(wl) * wl.n_streams * wl.T
-            self.kernel = f"decode_kernel<{wl.bank_dtype},{wl.idx_dtype},bulk>"
+            self.kernel = f"decode_vec_kernel<{wl.bank_dtype},{wl.idx_dtype}>"
             self.metric = METRIC
         else:
             wl = workloads.GATHER_WORKLOADS[name]
@@ -249,7 +249,7 @@ class Case:
             self.unit = "tokens/s"
             self.launches = 1
             self.nbytes = workloads.gather_bytes(wl, self.g["chunk_valid"])
-            self.kernel = f"gather_kernel<{wl.bank_dtype},{wl.idx_dtype},{wl.w_dtype},bulk>"
+            self.kernel = f"gather_kernel<{wl.bank_dtype},{wl.idx_dtype},{wl.w_dtype},vector rows>"
             self.metric = "SDM token-gather tokens/sec and effective bank GB/s as fraction of GB300 HBM peak"
         self.wl = wl
 
@@ -285,6 +285,31 @@ class Case:
     def e2e(self, steps: int, r: sdist.Rank) -> dict:
         dev, wl, sdm = self.dev, self.wl, self.sdm
         stream = torch.cuda.current_stream(dev)
+        if self.kind == "decode_seq":
+            # the package's host-fed decoder: double-buffered device inputs, copies on their own streams
+            from decode_state_gb300.hostfed import HostFedDecoder
+
+            host_in = {k: self.x[k].cpu().pin_memory() for k in DECODE_KEYS}
+            outs_h = [torch.empty(self.out.shape, dtype=self.out.dtype, pin_memory=True) for _ in range(2)]
+            dec = HostFedDecoder(self.x["bank"], self.x, depth=2)
+            h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+            d2h = outs_h[0].numel() * outs_h[0].element_size()
+            for i in range(3):
+                dec.submit(host_in, outs_h[i % 2])
+            dec.synchronize()
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            sdist.barrier(r, dev)
+            e0.record(dec.h2d)
+            for i in range(steps):
+                dec.submit(host_in, outs_h[i % 2])
+            e1.record(dec.d2h)
+            dec.synchronize()
+            torch.cuda.synchronize()
+            ms = sdist.max_over_ranks(r, e0.elapsed_time(e1), dev)
+            return {"value": self.units * steps * r.world / (ms / 1e3), "unit": self.unit, "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "steps": steps, "ms_per_step": ms / steps,
+                    "api": "decode_state_gb300.hostfed.HostFedDecoder (depth 2)"}
         if self.kind.startswith("decode"):
             host_in = [self.x[k].cpu().pin_memory() for k in DECODE_KEYS]
             dev_in = [torch.empty_like(self.x[k]) for k in DECODE_KEYS]

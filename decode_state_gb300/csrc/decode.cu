@@ -15,17 +15,21 @@
 // the reference kernel makes for its CTA barrier).
 //
 // Vector path (rows a multiple of 16 bytes), per token:
-//   1. warp 0 issues one bulk copy (cp.async.bulk, async proxy) per write row slice into shared
-//      memory, all in flight at once, completion counted on an mbarrier; meanwhile every thread
-//      issues cp.async copies of the NEXT token's slots and weights, and thread 0 computes the next
-//      token's shared gate;
+//   1. every thread issues 16-byte cp.async copies of the W write row slices into shared memory
+//      (all in flight at once), then cp.async copies of the NEXT token's slots and weights, and
+//      thread 0 computes the next token's shared gate;
 //   2. each thread owns two adjacent columns, held as a packed float32 pair, and runs the
 //      retrieve as one chain of paired fmas over ascending w, then delta, then the decay-and-write
 //      (paired multiply and fma, one paired round to the bank dtype, one store per row);
-//   3. fence.proxy.async.global + barrier, then warp 0 bulk-copies the R read rows and each thread
-//      reduces its columns over ascending r;
+//   3. a barrier, then the R read rows by 16-byte cp.async, and each thread reduces its columns
+//      over ascending r;
 //   4. the prefetched metadata of the next token is turned into row byte offsets and broadcast
 //      weight pairs in shared memory.
+// The rows travel as 16-byte cp.async copies (the load/store path, generic proxy) rather than one
+// bulk copy per row: with 256-byte rows the bulk-copy engine sustained about 3 TB/s of row reads
+// per GPU, the 16-byte copies spread over all threads sustain the rest of HBM. Being generic-proxy
+// copies, they see the block's earlier stores after a plain barrier, and no wait in this file
+// spins.
 // Rows that are not a multiple of 16 bytes (or unaligned pointers) take a plain-load path with
 // one column per thread; a thread then only ever touches its own column, so program order alone
 // orders its writes and reads.
@@ -93,8 +97,7 @@ struct Pair<float> {
 // ---------------------------------------------------------------- vector-path layout
 
 struct VecLayout {
-    size_t rows, raw_k, raw_kv, raw_g, raw_q, raw_qv, raw_beta, koff, qoff, aw2, kv2, dw2, qv2, beta, dnext, bar,
-        total;
+    size_t rows, raw_k, raw_kv, raw_g, raw_q, raw_qv, raw_beta, koff, qoff, aw2, kv2, dw2, qv2, beta, dnext, total;
     __host__ __device__ VecLayout(int W, int R, int G, int sw, int es, int is) {
         const int maxwr = W > R ? W : R;
         rows = 0;
@@ -112,8 +115,7 @@ struct VecLayout {
         qv2 = dw2 + (size_t)W * 8;
         beta = qv2 + (size_t)R * 8;
         dnext = beta + 4;
-        bar = align_up(dnext + 4, 8);
-        total = bar + 8;
+        total = dnext + 4;
     }
 };
 
@@ -191,39 +193,38 @@ __device__ __forceinline__ void derive_meta(const DecodeArgs& a, int c0, const V
     if (tid == 0) *reinterpret_cast<float*>(smem + L.beta) = *reinterpret_cast<const float*>(smem + L.raw_beta);
 }
 
-// Warp 0: bulk-copy n row slices (row_bytes each) at byte offsets off[] into rows[i * sw].
+// Every thread: 16-byte cp.async copies (LSU path, generic proxy) of n row slices at byte offsets
+// off[] into rows[i * sw]; one commit group.
 template <typename E>
-__device__ __forceinline__ void issue_rows_off(E* rows, const unsigned char* bank, const int64_t* off, int n, int sw,
-                                               uint32_t row_bytes, uint64_t* bar) {
-    const int lane = threadIdx.x;
-    if (lane == 0) mbar_arrive_expect_tx(bar, row_bytes * (uint32_t)n);
-    __syncwarp();
-    for (int i = lane; i < n; i += 32) bulk_g2s(rows + (size_t)i * sw, bank + off[i], row_bytes, bar);
-}
-
-// Wait for the current bulk phase; on a timeout every thread of the block learns it at the
-// barrier, the block records SDM_DEV_TIMEOUT, waits once more (bounded) for its copies and
-// reports that it must stop.
-__device__ __forceinline__ bool wait_phase(uint64_t* bar, uint32_t& parity, int* s_abort) {
-    const bool ok = mbar_wait_bounded(bar, parity, kWaitLimitNs);
-    if (!ok) atomicOr(s_abort, 1);
-    __syncthreads();
-    if (*s_abort) {
-        if (threadIdx.x == 0) atomicOr(&g_decode_status, SDM_DEV_TIMEOUT);
-        if (!ok) mbar_wait_bounded(bar, parity, kWaitLimitNs);
-        return false;
+__device__ __forceinline__ void ldgsts_rows(E* rows, const unsigned char* bank, const int64_t* off, int n, int sw,
+                                            uint32_t row_bytes) {
+    const int tid = threadIdx.x, nt = blockDim.x;
+    const int cpr = (int)(row_bytes >> 4);  // 16-byte chunks per row slice
+    unsigned char* dst = reinterpret_cast<unsigned char*>(rows);
+    const size_t rs = (size_t)sw * sizeof(E);
+    if (nt % cpr == 0) {
+        const int k = tid % cpr, step = nt / cpr;
+        for (int r = tid / cpr; r < n; r += step)
+            asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst + r * rs + k * 16)),
+                         "l"(bank + off[r] + k * 16)
+                         : "memory");
+    } else {
+        for (int c = tid; c < n * cpr; c += nt) {
+            const int r = c / cpr, k = c - r * cpr;
+            asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst + r * rs + k * 16)),
+                         "l"(bank + off[r] + k * 16)
+                         : "memory");
+        }
     }
-    parity ^= 1u;
-    return true;
+    cp_async_commit();
 }
 
 template <typename E, typename I>
-__global__ void __launch_bounds__(kMaxThreads, 2) decode_vec_kernel(const DecodeArgs a) {
+__global__ void __launch_bounds__(kMaxThreads, 2) decode_vec_kernel(const DecodeArgs a, int early_trigger) {
     using P = Pair<E>;
     using PT = typename P::T;
     constexpr int ES = sizeof(E);
     extern __shared__ __align__(128) unsigned char smem[];
-    __shared__ int s_abort;
 
     const int W = a.W, R = a.R, G = a.G, hd = a.hd, sw = a.slice_cols;
     const VecLayout L(W, R, G, sw, ES, (int)sizeof(I));
@@ -234,7 +235,6 @@ __global__ void __launch_bounds__(kMaxThreads, 2) decode_vec_kernel(const Decode
     const uint64_t* kv2 = reinterpret_cast<const uint64_t*>(smem + L.kv2);
     const uint64_t* dw2 = reinterpret_cast<const uint64_t*>(smem + L.dw2);
     const uint64_t* qv2 = reinterpret_cast<const uint64_t*>(smem + L.qv2);
-    uint64_t* bar = reinterpret_cast<uint64_t*>(smem + L.bar);
 
     const int tid = threadIdx.x;
     const int64_t s = blockIdx.x / a.n_slices;
@@ -249,11 +249,8 @@ __global__ void __launch_bounds__(kMaxThreads, 2) decode_vec_kernel(const Decode
     const PT* rp = reinterpret_cast<const PT*>(rows) + tid;
     const int64_t jb = (int64_t)j * ES;
 
-    if (tid == 0) {
-        s_abort = 0;
-        mbar_init(bar, 1);
-        mbar_init_fence();
-    }
+    grid_dependency_wait();
+    if (early_trigger) grid_launch_dependents();
     prefetch_meta<I>(a, s, L, smem);  // token 0
     cp_async_wait_all();
     __syncthreads();
@@ -262,13 +259,12 @@ __global__ void __launch_bounds__(kMaxThreads, 2) decode_vec_kernel(const Decode
     __syncthreads();
     derive_meta<E, I>(a, c0, L, smem);
     __syncthreads();
-    uint32_t parity = 0;
 
     for (int t = 0; t < a.T; ++t) {
         const int64_t ts = (int64_t)t * a.n_streams + s;  // (token, stream) row of the time-major inputs
 
         // 1. the write rows; the next token's metadata meanwhile
-        if (tid < 32) issue_rows_off<E>(rows, bank, koff, W, sw, row_bytes, bar);
+        ldgsts_rows<E>(rows, bank, koff, W, sw, row_bytes);
         uint64_t vr = 0;
         if (active) {
             const float2 vv = __ldg(reinterpret_cast<const float2*>(a.v + ts * hd + c0 + j));
@@ -276,12 +272,17 @@ __global__ void __launch_bounds__(kMaxThreads, 2) decode_vec_kernel(const Decode
         }
         const float beta = *reinterpret_cast<const float*>(smem + L.beta);
         const uint64_t dsh = dw2[0];
-        if (t + 1 < a.T) {
+        const bool more = t + 1 < a.T;
+        if (more) {
             prefetch_meta<I>(a, ts + a.n_streams, L, smem);
             if (G == 1 && tid == 0)  // the next token's shared gate, while this token's rows are in flight
                 *reinterpret_cast<float*>(smem + L.dnext) = (float)exp((double)__ldg(a.g + ts + a.n_streams));
         }
-        if (!wait_phase(bar, parity, &s_abort)) return;
+        if (more)
+            asm volatile("cp.async.wait_group 1;" ::: "memory");  // the rows, not yet the metadata
+        else
+            cp_async_wait_all();
+        __syncthreads();
 
         // 2. retrieve, delta, decay-and-write
         if (active) {
@@ -306,12 +307,12 @@ __global__ void __launch_bounds__(kMaxThreads, 2) decode_vec_kernel(const Decode
                 *reinterpret_cast<PT*>(bank + koff[w] + jb) = P::narrow(y);
             }
         }
-        fence_proxy_async_global();
         __syncthreads();
 
         // 3. the read rows, after the write
-        if (tid < 32) issue_rows_off<E>(rows, bank, qoff, R, sw, row_bytes, bar);
-        if (!wait_phase(bar, parity, &s_abort)) return;
+        ldgsts_rows<E>(rows, bank, qoff, R, sw, row_bytes);
+        cp_async_wait_all();
+        __syncthreads();
         if (active) {
             uint64_t acc = 0;
             int r = 0;
@@ -334,6 +335,7 @@ __global__ void __launch_bounds__(kMaxThreads, 2) decode_vec_kernel(const Decode
         __syncthreads();
     }
 }
+
 
 // ---------------------------------------------------------------- plain-load path
 
@@ -368,7 +370,7 @@ __device__ __forceinline__ void load_rows_simt(E* rows, const E* bank, const int
 }
 
 template <typename E, typename I>
-__global__ void __launch_bounds__(kMaxThreads) decode_simt_kernel(const DecodeArgs a) {
+__global__ void __launch_bounds__(kMaxThreads) decode_simt_kernel(const DecodeArgs a, int early_trigger) {
     constexpr int ES = sizeof(E);
     extern __shared__ __align__(128) unsigned char smem[];
 
@@ -390,6 +392,8 @@ __global__ void __launch_bounds__(kMaxThreads) decode_simt_kernel(const DecodeAr
     const bool active = j < ncols;
     E* bank = static_cast<E*>(a.bank);
     E* out = static_cast<E*>(a.out);
+    grid_dependency_wait();
+    if (early_trigger) grid_launch_dependents();
 
     for (int t = 0; t < a.T; ++t) {
         const int64_t ts = (int64_t)t * a.n_streams + s;
@@ -430,20 +434,11 @@ __global__ void __launch_bounds__(kMaxThreads) decode_simt_kernel(const DecodeAr
 
 // ---------------------------------------------------------------- launch
 
-template <typename K>
-int launch_kernel(K kernel, const DecodeArgs& a, dim3 grid, dim3 block, size_t smem, cudaStream_t stream) {
-    if (smem > 48 * 1024) {  // opt in to more than the default dynamic shared memory
-        const cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return (int)e;
-    }
-    kernel<<<grid, block, smem, stream>>>(a);
-    return (int)cudaGetLastError();
-}
-
 template <typename E, typename I>
 int launch_typed(bool vec, const DecodeArgs& a, dim3 grid, dim3 block, size_t smem, cudaStream_t stream) {
-    return vec ? launch_kernel(decode_vec_kernel<E, I>, a, grid, block, smem, stream)
-               : launch_kernel(decode_simt_kernel<E, I>, a, grid, block, smem, stream);
+    const auto kernel = vec ? decode_vec_kernel<E, I> : decode_simt_kernel<E, I>;
+    const int early = fits_one_wave(kernel, grid.x, (int)block.x, smem) ? 1 : 0;
+    return launch_pdl(kernel, grid, block, smem, stream, a, early);
 }
 
 int shrink_cols(int sw, int q) {

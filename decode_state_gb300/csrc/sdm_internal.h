@@ -50,4 +50,43 @@ int gather_status(unsigned int* word, bool clear);
 // Multiprocessor count of the current device (cached per device).
 int sm_count();
 
+// Launch `kernel` with programmatic stream serialization (see grid_dependency_wait). Returns a
+// cudaError_t. Raises the dynamic shared-memory limit first when smem exceeds the default 48 KB.
+template <typename... P, typename... A>
+int launch_pdl(void (*kernel)(P...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream, A... args) {
+    if (smem > 48 * 1024) {
+        const cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) {
+            (void)cudaGetLastError();
+            return (int)e;
+        }
+    }
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, args...);
+    if (e == cudaSuccess) e = cudaGetLastError();
+    else (void)cudaGetLastError();
+    return (int)e;
+}
+
+// True when all `blocks` of `kernel` can be resident at once, so that blocks of the next kernel
+// scheduled early cannot take the place of blocks of this one.
+template <typename... P>
+bool fits_one_wave(void (*kernel)(P...), int64_t blocks, int threads, size_t smem) {
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, smem) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return false;
+    }
+    return blocks <= (int64_t)per_sm * sm_count();
+}
+
 }  // namespace sdm

@@ -17,6 +17,9 @@
  *     slots must be private to it and its W write slots distinct (none of this is checked, as in
  *     the reference). The gather knows the bank's row count and skips out-of-range rows, raising
  *     SDM_DEV_BAD_INDEX in the device status word (sdm_device_status).
+ *   - Launches use programmatic stream serialization: a kernel may be scheduled while the previous
+ *     kernel on the stream is still finishing, but it reads and writes no memory before that kernel
+ *     has completed (griddepcontrol.wait), so stream order is kept.
  *   - bfloat16 data is raw 16-bit patterns (the high half of an IEEE float32).
  *   - Results are deterministic: every sum is accumulated in a fixed order independent of the GPU.
  *
@@ -58,7 +61,7 @@ typedef struct CUstream_st* sdm_stream_t;
 #define SDM_ENOPS (-11)     /* gather operand count is not 1 or 2 */
 
 /* bits of the device status word */
-#define SDM_DEV_TIMEOUT 1u   /* a kernel gave up waiting for its own row copies (never expected) */
+#define SDM_DEV_TIMEOUT 1u   /* reserved: a kernel gave up a bounded wait (no current kernel waits) */
 #define SDM_DEV_BAD_INDEX 2u /* the gather met a row index outside [0, n_slots) and skipped it */
 
 /*

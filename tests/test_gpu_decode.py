@@ -177,3 +177,44 @@ def test_full_size_steps_bf16_gw():
         for t0 in range(0, wl.T, 16):
             assert_close(got[t0:t0 + 16], ref[t0:t0 + 16], "bf16", f"stream {s} tokens {t0}..{t0 + 15}")
         assert_close(to_np(x["bank"][s * P:(s + 1) * P]), ref_bank, "bf16", f"slots of stream {s}")
+
+
+def test_layer_state_steps_match_seq_and_oracle():
+    from decode_state_gb300.state import SDMLayerState
+
+    wl = _wl("bf16", "i64", 6, 96, 64, 8, 5, "W", 4, seed=9)
+    x = workloads.make_decode_inputs(wl, device=DEV)
+    bank_ref, out_ref = _oracle_seq(x)
+    st = SDMLayerState(x["bank"].clone())
+    outs = [st.step(*(x[k][t] for k in DECODE_KEYS)) for t in range(wl.T)]
+    assert st.cache_len == wl.T
+    seq = SDMLayerState(x["bank"].clone(), seq_len=2)
+    out_seq = seq.steps(*(x[k] for k in DECODE_KEYS))
+    torch.cuda.synchronize()
+    assert seq.cache_len == 2 + wl.T
+    assert torch.equal(torch.stack(outs).view(torch.int16), out_seq.view(torch.int16))
+    assert torch.equal(st.memory.view(torch.int16), seq.memory.view(torch.int16))
+    assert_close(to_np(out_seq), out_ref, "bf16", "readings")
+    assert_close(to_np(seq.memory), bank_ref, "bf16", "bank")
+
+
+def test_host_fed_decoder_matches_sequential_calls():
+    """Pipelined host-fed steps (double-buffered inputs, copies on their own streams) give the same
+    bank and readings, bit for bit, as the same steps run one after another on the device."""
+    from decode_state_gb300.hostfed import HostFedDecoder
+
+    wl = _wl("bf16", "i32", 40, 128, 128, 16, 16, 1, 4, seed=11)
+    steps = [workloads.make_decode_inputs(wl, device=DEV, seed=100 + n) for n in range(5)]
+    bank0 = steps[0]["bank"].clone()
+    ref_bank = bank0.clone()
+    refs = [sdm.decode_seq(ref_bank, *(x[k] for k in DECODE_KEYS)).clone() for x in steps]
+    dec = HostFedDecoder(bank0, steps[0], depth=2)
+    host = [{k: x[k].cpu().pin_memory() for k in DECODE_KEYS} for x in steps]
+    outs = [torch.empty(refs[0].shape, dtype=torch.bfloat16, pin_memory=True) for _ in steps]
+    for h, o in zip(host, outs):
+        dec.submit(h, o)
+    dec.synchronize()
+    torch.cuda.synchronize()
+    for o, ref in zip(outs, refs):
+        assert torch.equal(o.view(torch.int16), ref.cpu().view(torch.int16))
+    assert torch.equal(bank0.view(torch.int16), ref_bank.view(torch.int16))
