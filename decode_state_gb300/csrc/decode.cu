@@ -337,6 +337,170 @@ __global__ void __launch_bounds__(kMaxThreads, 2) decode_vec_kernel(const Decode
 }
 
 
+// ---------------------------------------------------------------- streaming path (wide rows)
+// When W or R rows do not fit the shared-memory budget at a useful slice width (e.g. 256 rows of
+// 1 KiB), the rows stream through a ring of NS chunk buffers of CH rows each instead of being
+// staged all at once: the write rows pass twice (retrieve, then decay-and-write; the second pass
+// is served mostly by L2) and the read rows once. Chunks are consumed in ascending row order, so
+// every sum keeps the order and the bits of the staged path.
+
+constexpr int kStreamRows = 16;   // rows per chunk
+constexpr int kStreamStages = 4;  // chunk buffers in the ring
+
+struct StreamLayout {
+    VecLayout meta;  // the metadata of the staged layout, with no row area
+    size_t ring, total;
+    __host__ __device__ StreamLayout(int W, int R, int G, int sw, int es, int is) : meta(W, R, G, 0, es, is) {
+        ring = align_up(meta.total, 128);
+        total = ring + (size_t)kStreamStages * kStreamRows * sw * es;
+    }
+};
+
+// Every thread: rows [r0, r0 + n) of off[] into ring buffer dst; one commit group.
+template <typename E>
+__device__ __forceinline__ void ldgsts_chunk(unsigned char* dst, const unsigned char* bank, const int64_t* off, int r0,
+                                             int n, int sw, uint32_t row_bytes) {
+    ldgsts_rows<E>(reinterpret_cast<E*>(dst), bank, off + r0, n, sw, row_bytes);
+}
+
+template <typename E, typename I>
+__global__ void __launch_bounds__(kMaxThreads, 1) decode_stream_kernel(const DecodeArgs a, int early_trigger) {
+    using P = Pair<E>;
+    using PT = typename P::T;
+    constexpr int ES = sizeof(E);
+    constexpr int NS = kStreamStages, CH = kStreamRows;
+    extern __shared__ __align__(128) unsigned char smem[];
+
+    const int W = a.W, R = a.R, G = a.G, hd = a.hd, sw = a.slice_cols;
+    const StreamLayout SL(W, R, G, sw, ES, (int)sizeof(I));
+    const VecLayout& L = SL.meta;
+    unsigned char* ring = smem + SL.ring;
+    const size_t stage_bytes = (size_t)CH * sw * ES;
+    const int64_t* koff = reinterpret_cast<const int64_t*>(smem + L.koff);
+    const int64_t* qoff = reinterpret_cast<const int64_t*>(smem + L.qoff);
+    const uint64_t* aw2 = reinterpret_cast<const uint64_t*>(smem + L.aw2);
+    const uint64_t* kv2 = reinterpret_cast<const uint64_t*>(smem + L.kv2);
+    const uint64_t* dw2 = reinterpret_cast<const uint64_t*>(smem + L.dw2);
+    const uint64_t* qv2 = reinterpret_cast<const uint64_t*>(smem + L.qv2);
+
+    const int tid = threadIdx.x;
+    const int64_t s = blockIdx.x / a.n_slices;
+    const int c0 = (int)(blockIdx.x % a.n_slices) * sw;
+    const int ncols = min(sw, hd - c0);
+    const int j = 2 * tid;
+    const bool active = j < ncols;
+    const uint32_t row_bytes = (uint32_t)ncols * ES;
+    const int pstride = sw / 2;
+    unsigned char* bank = static_cast<unsigned char*>(a.bank);
+    E* out = static_cast<E*>(a.out);
+    const int64_t jb = (int64_t)j * ES;
+    const int nk = (W + CH - 1) / CH, nq = (R + CH - 1) / CH;
+    // row pair of this thread in row r of ring stage st
+    const auto at = [&](int st, int r) -> PT {
+        return reinterpret_cast<const PT*>(ring + st * stage_bytes)[r * pstride + tid];
+    };
+
+    grid_dependency_wait();
+    if (early_trigger) grid_launch_dependents();
+    prefetch_meta<I>(a, s, L, smem);  // token 0
+    cp_async_wait_all();
+    __syncthreads();
+    if (G == 1 && tid == 0)
+        *reinterpret_cast<float*>(smem + L.dnext) = (float)exp((double)*reinterpret_cast<const float*>(smem + L.raw_g));
+    __syncthreads();
+    derive_meta<E, I>(a, c0, L, smem);
+    __syncthreads();
+
+    for (int t = 0; t < a.T; ++t) {
+        const int64_t ts = (int64_t)t * a.n_streams + s;
+        uint64_t vr = 0;
+        if (active) {
+            const float2 vv = __ldg(reinterpret_cast<const float2*>(a.v + ts * hd + c0 + j));
+            vr = P::widen(P::narrow(f2(vv.x, vv.y)));
+        }
+        const float beta = *reinterpret_cast<const float*>(smem + L.beta);
+        const uint64_t dsh = dw2[0];
+
+        // passes 1 and 2: job q < nk retrieves over write chunk q; job q >= nk writes chunk q - nk
+        uint64_t acc = 0, delta = 0;
+        const int jobs = 2 * nk;
+        // exactly NS - 1 groups ahead (empty ones past the last job), so that after job q's own
+        // group the wait for "at most NS - 1 pending" always covers job q
+        for (int q = 0; q < NS - 1; ++q) {
+            if (q < jobs) {
+                const int c = q % nk;
+                ldgsts_chunk<E>(ring + (q % NS) * stage_bytes, bank, koff, c * CH, min(CH, W - c * CH), sw, row_bytes);
+            } else {
+                cp_async_commit();
+            }
+        }
+        for (int q = 0; q < jobs; ++q) {
+            const int qn = q + NS - 1;
+            if (qn < jobs) {
+                const int c = qn % nk;
+                ldgsts_chunk<E>(ring + (qn % NS) * stage_bytes, bank, koff, c * CH, min(CH, W - c * CH), sw, row_bytes);
+            } else {
+                cp_async_commit();  // keep one group per job
+            }
+            asm volatile("cp.async.wait_group %0;" ::"n"(NS - 1) : "memory");
+            __syncthreads();
+            const int st = q % NS, c = q % nk, r0 = c * CH, n = min(CH, W - r0);
+            if (active) {
+                if (q < nk) {
+                    for (int r = 0; r < n; ++r) acc = ffma2(aw2[r0 + r], P::widen(at(st, r)), acc);
+                } else {
+                    if (q == nk) {
+                        const float dl = __fmul_rn(beta, __fsub_rn(f2lo(vr), f2lo(acc)));
+                        const float dh = __fmul_rn(beta, __fsub_rn(f2hi(vr), f2hi(acc)));
+                        delta = f2(dl, dh);
+                    }
+                    for (int r = 0; r < n; ++r) {
+                        const int w = r0 + r;
+                        const uint64_t y = ffma2(kv2[w], delta, fmul2(P::widen(at(st, r)), G == 1 ? dsh : dw2[w]));
+                        *reinterpret_cast<PT*>(bank + koff[w] + jb) = P::narrow(y);
+                    }
+                }
+            }
+            __syncthreads();  // stage st is refilled by the next iteration's copy
+        }
+
+        // pass 3: the read rows, after every write of this token; the next token's metadata too
+        const bool more = t + 1 < a.T;
+        if (more) {
+            prefetch_meta<I>(a, ts + a.n_streams, L, smem);
+            if (G == 1 && tid == 0)
+                *reinterpret_cast<float*>(smem + L.dnext) = (float)exp((double)__ldg(a.g + ts + a.n_streams));
+        }
+        uint64_t racc = 0;
+        for (int q = 0; q < NS - 1; ++q) {
+            if (q < nq)
+                ldgsts_chunk<E>(ring + (q % NS) * stage_bytes, bank, qoff, q * CH, min(CH, R - q * CH), sw, row_bytes);
+            else
+                cp_async_commit();
+        }
+        for (int q = 0; q < nq; ++q) {
+            const int qn = q + NS - 1;
+            if (qn < nq)
+                ldgsts_chunk<E>(ring + (qn % NS) * stage_bytes, bank, qoff, qn * CH, min(CH, R - qn * CH), sw, row_bytes);
+            else
+                cp_async_commit();
+            asm volatile("cp.async.wait_group %0;" ::"n"(NS - 1) : "memory");
+            __syncthreads();
+            const int st = q % NS, r0 = q * CH, n = min(CH, R - r0);
+            if (active)
+                for (int r = 0; r < n; ++r) racc = ffma2(qv2[r0 + r], P::widen(at(st, r)), racc);
+            __syncthreads();
+        }
+        if (active) *reinterpret_cast<PT*>(out + ts * hd + c0 + j) = P::narrow(racc);
+
+        // the next token's metadata
+        cp_async_wait_all();
+        __syncthreads();
+        if (more) derive_meta<E, I>(a, c0, L, smem);
+        __syncthreads();
+    }
+}
+
 // ---------------------------------------------------------------- plain-load path
 
 struct SimtLayout {
@@ -434,9 +598,13 @@ __global__ void __launch_bounds__(kMaxThreads) decode_simt_kernel(const DecodeAr
 
 // ---------------------------------------------------------------- launch
 
+enum Path { kSimt = 0, kStaged = 1, kStream = 2 };
+
 template <typename E, typename I>
-int launch_typed(bool vec, const DecodeArgs& a, dim3 grid, dim3 block, size_t smem, cudaStream_t stream) {
-    const auto kernel = vec ? decode_vec_kernel<E, I> : decode_simt_kernel<E, I>;
+int launch_typed(int path, const DecodeArgs& a, dim3 grid, dim3 block, size_t smem, cudaStream_t stream) {
+    const auto kernel = path == kStaged ? decode_vec_kernel<E, I>
+                        : path == kStream ? decode_stream_kernel<E, I>
+                                          : decode_simt_kernel<E, I>;
     const int early = fits_one_wave(kernel, grid.x, (int)block.x, smem) ? 1 : 0;
     return launch_pdl(kernel, grid, block, smem, stream, a, early);
 }
@@ -461,10 +629,14 @@ int launch_decode(const DecodeArgs& a0, int bank_dtype, int idx_dtype, cudaStrea
     const int maxwr = std::max(a.W, a.R);
 
     // Column slice: the whole row when it fits; narrower to bound shared memory and to give the
-    // grid at least two blocks per SM when there are few streams.
-    int sw = std::min(a.hd, kMaxThreads * cpt);
-    if (vec) sw = sw / q * q;
+    // grid at least two blocks per SM when there are few streams. When staging every row would
+    // force slices narrower than 256 bytes (wide rows with many writes or reads), the rows stream
+    // through a chunk ring instead, with slices of up to 512 bytes.
+    const int full = vec ? std::min(a.hd, kMaxThreads * cpt) / q * q : std::min(a.hd, kMaxThreads * cpt);
+    int sw = full;
     while ((size_t)maxwr * sw * es > kRowsBudget && sw > q) sw = shrink_cols(sw, q);
+    const bool streamed = vec && (int64_t)sw * es < std::min<int64_t>((int64_t)full * es, 256);
+    if (streamed) sw = std::min(full, 512 / es) / q * q;
     const int64_t want_blocks = 2LL * sm_count();
     while (a.n_streams * ((a.hd + sw - 1) / sw) < want_blocks && sw * es > 128) {
         const int next = shrink_cols(sw, q);
@@ -476,15 +648,18 @@ int launch_decode(const DecodeArgs& a0, int bank_dtype, int idx_dtype, cudaStrea
     const int64_t blocks = a.n_streams * a.n_slices;
     if (blocks > INT_MAX) return SDM_ECOUNT;
     const int threads = ((sw + cpt - 1) / cpt + 31) / 32 * 32;
-    const size_t smem = vec ? VecLayout(a.W, a.R, a.G, sw, es, is).total : SimtLayout(a.W, a.R, sw, es).total;
+    const int path = !vec ? kSimt : streamed ? kStream : kStaged;
+    const size_t smem = path == kStaged   ? VecLayout(a.W, a.R, a.G, sw, es, is).total
+                        : path == kStream ? StreamLayout(a.W, a.R, a.G, sw, es, is).total
+                                          : SimtLayout(a.W, a.R, sw, es).total;
 
     const dim3 grid((unsigned)blocks), block((unsigned)threads);
     if (bank_dtype == SDM_BF16) {
-        return idx_dtype == SDM_I32 ? launch_typed<uint16_t, int32_t>(vec, a, grid, block, smem, stream)
-                                    : launch_typed<uint16_t, int64_t>(vec, a, grid, block, smem, stream);
+        return idx_dtype == SDM_I32 ? launch_typed<uint16_t, int32_t>(path, a, grid, block, smem, stream)
+                                    : launch_typed<uint16_t, int64_t>(path, a, grid, block, smem, stream);
     }
-    return idx_dtype == SDM_I32 ? launch_typed<float, int32_t>(vec, a, grid, block, smem, stream)
-                                : launch_typed<float, int64_t>(vec, a, grid, block, smem, stream);
+    return idx_dtype == SDM_I32 ? launch_typed<float, int32_t>(path, a, grid, block, smem, stream)
+                                : launch_typed<float, int64_t>(path, a, grid, block, smem, stream);
 }
 
 int decode_status(unsigned int* word, bool clear) {

@@ -46,6 +46,8 @@ SMALL = [
     ("bf16", "i32", 33, 128, 128, 64, 64, 1, 5),    # the serving shape, fewer streams
     ("bf16", "i64", 1, 64, 8, 1, 1, 1, 3),          # W = R = 1, 16-byte rows
     ("f32", "i32", 2, 16, 1, 4, 4, "W", 3),         # head_dim 1
+    ("f32", "i64", 5, 300, 256, 40, 7, 1, 3),       # streamed rows: 3 write chunks, 1 read chunk
+    ("bf16", "i32", 3, 400, 512, 70, 200, "W", 2),  # streamed rows: 1 KiB rows in 512-byte slices
 ]
 IDS = [f"{c[0]}-{c[1]}-S{c[2]}-hd{c[4]}-W{c[5]}R{c[6]}G{c[7]}-T{c[8]}" for c in SMALL]
 
