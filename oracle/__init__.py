@@ -92,6 +92,8 @@ class Oracle:
         lib.oracle_sdm_gather.argtypes = [vp, i32, i64, i64, i32, vp, vp, vp, i32, vp, vp, vp, i32,
                                           i32, i32, vp, i64, i32, i32, vp, i32, i32]
         lib.oracle_sdm_gather.restype = i32
+        lib.oracle_sdm_gather_kpos.argtypes = [vp, i32, i64, i64, vp, i32, i32, vp, vp, i64, i32, i32, vp, i32]
+        lib.oracle_sdm_gather_kpos.restype = i32
         lib.oracle_f32_to_bf16_array.argtypes = [vp, vp, i64]
         lib.oracle_f32_to_bf16_array.restype = None
         lib.oracle_bf16_to_f32_array.argtypes = [vp, vp, i64]
@@ -162,6 +164,32 @@ class Oracle:
             raise OracleError("oracle_sdm_gather", rc)
         return out0, out1, st
 
+    def gather_kpos(self, bank, idx0, kpos, compact, *, chunk: int, valid: int = -1, chunk_valid=None,
+                    check: bool = True):
+        """Compact snapshot of operand 0 (kpos form), written into ``compact`` in place.
+
+        compact [tokens / chunk, chunk * width0, hd] in the bank dtype; kpos [tokens, width0] int32,
+        -1 for entries that store nothing. Returns ``compact``.
+        """
+        n_slots, hd = bank.shape
+        tokens, width0 = idx0.shape
+        if valid < 0:
+            valid = chunk
+        if not compact.flags["C_CONTIGUOUS"] or compact.dtype != bank.dtype:
+            raise ValueError("compact must be C-contiguous in the bank dtype")
+        if compact.size != (tokens // chunk) * chunk * width0 * hd:
+            raise ValueError("compact must hold tokens / chunk blocks of chunk * width0 rows")
+        cv = None if chunk_valid is None else np.ascontiguousarray(chunk_valid, dtype=np.int32)
+        bank = np.ascontiguousarray(bank)
+        idx0 = np.ascontiguousarray(idx0)
+        kpos = np.ascontiguousarray(kpos, dtype=np.int32)
+        rc = self.lib.oracle_sdm_gather_kpos(_ptr(bank), _bank_code(bank), n_slots, hd, _ptr(idx0), width0,
+                                             _idx_code(idx0), _ptr(kpos), _ptr(compact), tokens, chunk, valid,
+                                             _ptr(cv), 1 if check else 0)
+        if rc != OK:
+            raise OracleError("oracle_sdm_gather_kpos", rc)
+        return compact
+
     def f32_to_bf16(self, x) -> np.ndarray:
         """float32 array -> bf16 bits (uint16), round to nearest even."""
         x = np.ascontiguousarray(x, dtype=np.float32)
@@ -200,6 +228,10 @@ def decode_step(*a, **kw):
 
 def gather(*a, **kw):
     return default().gather(*a, **kw)
+
+
+def gather_kpos(*a, **kw):
+    return default().gather_kpos(*a, **kw)
 
 
 def f32_to_bf16(x):

@@ -20,6 +20,11 @@
  *   - cuda/gather_cuda.py, token_gather_kernel: entries of a token are split over `groups` row
  *     groups, group g taking entries g, g+groups, ... in order with fmaf; the group partials
  *     are summed in order.
+ *   - cuda/gather_cuda.py, the compact-snapshot variant (kpos): instead of the stash, operand 0's
+ *     rows go to a snapshot of chunk * W0 rows per chunk; entry (t, n) of a live token with
+ *     kpos[t, n] >= 0 stores bank[idx_0[t, n]] at snapshot row kpos[t, n] of chunk t / chunk
+ *     (its first position in the chunk's sorted rows); kpos = -1 entries and padding tokens store
+ *     nothing, and no other snapshot row is written.
  *
  * Readings of the pages where they leave a step open (each is listed in the design notes):
  *   - float32 -> bfloat16 is round-to-nearest-even (NaN stays NaN, made quiet).
@@ -290,4 +295,37 @@ int oracle_sdm_gather(const void* bank, int bank_dtype, int64_t n_slots, int64_t
     }
     free(part);
     return rc;
+}
+
+/* Compact snapshot (the gather's kpos form): compact is [tokens / chunk, chunk * width0, hd] in the
+ * bank dtype, kpos [tokens, width0] int32. Writes only the rows kpos names for live tokens. */
+int oracle_sdm_gather_kpos(const void* bank, int bank_dtype, int64_t n_slots, int64_t hd, const void* idx0,
+                           int width0, int idx_dtype, const int32_t* kpos, void* compact, int64_t tokens, int chunk,
+                           int valid, const int32_t* chunk_valid, int check) {
+    if (!bank || !idx0 || !kpos || !compact) return ORACLE_EARG;
+    if (bank_dtype != O_BF16 && bank_dtype != O_F32) return ORACLE_EARG;
+    if (idx_dtype != O_I32 && idx_dtype != O_I64) return ORACLE_EARG;
+    if (hd < 1 || n_slots < 1 || tokens < 0 || chunk < 1 || tokens % chunk != 0) return ORACLE_EARG;
+    if (!chunk_valid && (valid < 0 || valid > chunk)) return ORACLE_EARG;
+    if (width0 < 1 || width0 > 256) return ORACLE_EARG;
+    const size_t bes = bank_dtype == O_BF16 ? 2 : 4;
+    const int64_t crow = (int64_t)chunk * width0; /* snapshot rows per chunk */
+    for (int64_t t = 0; t < tokens; ++t) {
+        int v_t = chunk_valid ? chunk_valid[t / chunk] : valid;
+        if (v_t < 0 || v_t > chunk) return ORACLE_EARG;
+        if ((int)(t % chunk) >= v_t) continue; /* padding: stores nothing */
+        for (int n = 0; n < width0; ++n) {
+            int32_t kp = kpos[t * width0 + n];
+            if (kp < 0) continue;
+            if (kp >= crow) {
+                if (check) return ORACLE_ERANGE;
+                continue;
+            }
+            int64_t slot = load_index(idx0, idx_dtype, t * width0 + n);
+            if (check && (slot < 0 || slot >= n_slots)) return ORACLE_ERANGE;
+            char* dst = (char*)compact + (size_t)(((t / chunk) * crow + kp) * hd) * bes;
+            memcpy(dst, (const char*)bank + (size_t)(slot * hd) * bes, (size_t)hd * bes);
+        }
+    }
+    return ORACLE_OK;
 }

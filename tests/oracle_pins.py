@@ -504,4 +504,59 @@ def pin_gather_scaling(orc):
     assert np.all(z == 0) and np.all(st == 0)
 
 
+def _sentinel_compact(n_chunks: int, crow: int, hd: int, dtype) -> np.ndarray:
+    c = np.empty((n_chunks, crow, hd), dtype=dtype)
+    c.view(np.uint8).fill(0xA5)
+    return c
+
+
+def pin_gather_kpos_hand(orc):
+    """Compact snapshot, float32 rows r_i = [i, -i], chunk 2, W0 = 2, 4 tokens (two chunks).
+    Chunk 0: token 0 slots [5, 3], token 1 slots [5, 7]; the chunk's sorted entries are 3, 5, 5, 7,
+    so kpos = [[1, 0], [-1, 3]] and the snapshot rows are r3, r5, (untouched), r7.
+    Chunk 1 (valid 1): token 2 slots [0, 0] with kpos [[0, -1]] writes r0 at row 0; token 3 is padding
+    and writes nothing although its kpos names rows 2 and 3."""
+    f = np.float32
+    bank = np.array([[i, -i] for i in range(8)], f)
+    idx = np.array([[5, 3], [5, 7], [0, 0], [1, 2]], np.int32)
+    kpos = np.array([[1, 0], [-1, 3], [0, -1], [2, 3]], np.int32)
+    comp = _sentinel_compact(2, 4, 2, f)
+    untouched = comp[0, 0].copy()
+    orc.gather_kpos(bank, idx, kpos, comp, chunk=2, chunk_valid=np.array([2, 1], np.int32))
+    assert comp[0, 0].tolist() == [3, -3] and comp[0, 1].tolist() == [5, -5] and comp[0, 3].tolist() == [7, -7]
+    assert comp[1, 0].tolist() == [0, 0]
+    for c, r in ((0, 2), (1, 1), (1, 2), (1, 3)):
+        assert_bits_equal(comp[c, r], untouched, f"untouched snapshot row {c},{r}")
+
+
+def pin_gather_kpos_first_occurrence(orc):
+    """kpos built from each chunk's sorted entries (numpy), first occurrence only: every named
+    snapshot row equals the bank row (numpy indexing), every other row keeps its old bits."""
+    rng = np.random.default_rng(15)
+    for dtype in ("bf16", "f32"):
+        n_slots, hd, tokens, chunk, W0 = 40, 6, 24, 4, 5
+        bank = to_bank(rng.normal(size=(n_slots, hd)), dtype)
+        idx = rng.integers(0, n_slots, size=(tokens, W0)).astype(np.int64)
+        cv = rng.integers(0, chunk + 1, size=tokens // chunk).astype(np.int32)
+        live = (np.arange(tokens) % chunk) < np.repeat(cv, chunk)
+        kpos = np.full((tokens, W0), -1, np.int32)
+        for c in range(tokens // chunk):
+            ent = idx[c * chunk:(c + 1) * chunk].ravel()
+            order = np.sort(ent)
+            seen = set()
+            for e, slot in enumerate(ent):
+                t = c * chunk + e // W0
+                if live[t] and slot not in seen:
+                    seen.add(slot)
+                    kpos[t, e % W0] = int(np.searchsorted(order, slot))
+        comp = _sentinel_compact(tokens // chunk, chunk * W0, hd, bank.dtype)
+        before = comp.copy()
+        orc.gather_kpos(bank, idx, kpos, comp, chunk=chunk, chunk_valid=cv)
+        named = np.zeros(comp.shape[:2], bool)
+        for t, n in zip(*np.nonzero(kpos >= 0)):
+            named[t // chunk, kpos[t, n]] = True
+            assert_bits_equal(comp[t // chunk, kpos[t, n]], bank[idx[t, n]], f"{dtype} snapshot row of ({t},{n})")
+        assert_bits_equal(comp[~named], before[~named], f"{dtype} rows no entry names")
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_") and callable(v)]

@@ -29,6 +29,10 @@ MUTANTS = {
                               "n < (gi + 1) * ((width + groups - 1) / groups); ++n) {"),
     "gather_padding_stash_kept": ("memset(dst, 0, (size_t)hd * bes);", "(void)dst;"),
     "gather_op1_uses_op0_weights": ("const void* w = o == 0 ? w0 : w1;", "const void* w = w0;"),
+    "kpos_padding_written": ("        if ((int)(t % chunk) >= v_t) continue; /* padding: stores nothing */",
+                             "        (void)v_t;"),
+    "kpos_row_of_entry_0": ("            int64_t slot = load_index(idx0, idx_dtype, t * width0 + n);\n            if (check && (slot",
+                            "            int64_t slot = load_index(idx0, idx_dtype, t * width0);\n            if (check && (slot"),
     "gather_padding_not_zeroed": ("for (int64_t c = 0; c < hd; ++c) out[t * hd + c] = 0.0f;",
                                   "for (int64_t c = 0; c < hd; ++c) out[t * hd + c] = out[t * hd + c];"),
 }
