@@ -72,24 +72,25 @@ def hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def kernel_source_hash() -> str:
+def kernel_source_hash(files) -> str:
+    """sha256 over the named kernel source files (name, NUL, bytes; sorted by name)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "decode_state_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
+    for f in sorted(files):
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(f.encode() + b"\0" + fh.read())
     return h.hexdigest()
 
 
 def ncu_traffic(workload: str):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken on the current kernels."""
+    """DRAM bytes per launch from the committed ncu record, if it was taken on the current sources."""
     path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     try:
         with open(path) as f:
             rec = json.load(f).get(workload)
-    except (OSError, ValueError):
-        return None
-    if not rec or rec.get("kernel_source_sha256") != kernel_source_hash():
+        if not rec or rec.get("kernel_source_sha256") != kernel_source_hash(rec["files"]):
+            return None
+    except (OSError, ValueError, KeyError):
         return None
     return rec.get("dram_bytes_per_launch")
 

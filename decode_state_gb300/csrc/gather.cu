@@ -16,6 +16,10 @@
 // about 3 TB/s of row reads per GPU. Rows that are not a multiple of 16 bytes, or an unaligned
 // bank, take a plain-load path with one column per thread. Row indices outside [0, n_slots) are
 // skipped (zero row) and flagged in the status word.
+//
+// Compact-snapshot form (kpos set): instead of the stash, operand 0's row of entry n goes to row
+// kpos[t, n] of the chunk's block of chunk * W0 rows when kpos >= 0; each thread stores the 16-byte
+// pieces it copied itself as soon as they have landed, so the form costs no extra barrier.
 #include <algorithm>
 #include <climits>
 
@@ -34,12 +38,13 @@ constexpr size_t kRowsBudget = 40 * 1024;
 __host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 struct GatherLayout {
-    size_t rows, slot, wt, total;
+    size_t rows, slot, wt, kp, total;
     __host__ __device__ GatherLayout(int n_rows, int slice_cols, int es) {
         rows = 0;
         slot = align_up((size_t)n_rows * slice_cols * es, 16);
         wt = slot + (size_t)n_rows * 8;
-        total = wt + (size_t)n_rows * 4;
+        kp = wt + (size_t)n_rows * 4;  // compact-snapshot rows of operand 0's entries
+        total = kp + (size_t)n_rows * 4;
     }
 };
 
@@ -70,7 +75,7 @@ __device__ void write_padding(const GatherArgs& a, int64_t t, int c0, int ncols,
 #pragma unroll
             for (int k = 0; k < CPT; ++k) a.out[1][t * hd + c0 + j + k] = 0.0f;
     }
-    if (a.stash == nullptr) return;
+    if (a.stash == nullptr || a.kpos != nullptr) return;  // the compact snapshot takes nothing from padding
     E* st = static_cast<E*>(a.stash) + t * W0 * hd;
     if (flat16) {  // the token's whole stash block is contiguous and 16-byte aligned
         uint4* p = reinterpret_cast<uint4*>(st);
@@ -95,6 +100,7 @@ __global__ void __launch_bounds__(kMaxThreads) gather_kernel(const GatherArgs a,
     E* rows = reinterpret_cast<E*>(smem + L.rows);
     int64_t* slot = reinterpret_cast<int64_t*>(smem + L.slot);
     float* wt = reinterpret_cast<float*>(smem + L.wt);
+    int* kp = reinterpret_cast<int*>(smem + L.kp);
 
     const int tid = threadIdx.x, nt = blockDim.x;
     const int64_t t = blockIdx.x / a.n_slices;
@@ -125,7 +131,17 @@ __global__ void __launch_bounds__(kMaxThreads) gather_kernel(const GatherArgs a,
         }
         slot[e] = sl;
         wt[e] = load_weight<WT>(op1 ? a.w[1] : a.w[0], i);
+        if (a.kpos != nullptr && !op1) {
+            int k = __ldg(a.kpos + i);
+            if (k >= a.chunk * W0 || (k >= 0 && sl < 0)) {
+                if (k >= a.chunk * W0) atomicOr(&g_gather_status, SDM_DEV_BAD_INDEX);
+                k = -1;
+            }
+            kp[e] = k;
+        }
     }
+    // compact snapshot: this token's chunk block
+    E* compact = a.kpos != nullptr ? stash + (t / a.chunk) * ((int64_t)a.chunk * W0) * hd : nullptr;
     __syncthreads();
 
     if (BULK) {
@@ -151,10 +167,23 @@ __global__ void __launch_bounds__(kMaxThreads) gather_kernel(const GatherArgs a,
             for (int c = tid; c < NR * cpr; c += nt) copy_chunk(c / cpr, c % cpr);
         }
         asm volatile("cp.async.commit_group;\n\tcp.async.wait_all;" ::: "memory");
+        if (compact != nullptr) {  // this thread's own landed pieces of operand 0's named rows
+            const auto put = [&](int e, int k) {
+                if (e < W0 && kp[e] >= 0)
+                    *reinterpret_cast<uint4*>(reinterpret_cast<unsigned char*>(compact) + kp[e] * rowb + c0 * ES +
+                                              k * 16) = *reinterpret_cast<const uint4*>(dst + e * rs + k * 16);
+            };
+            if (nt % cpr == 0) {
+                const int k = tid % cpr, step = nt / cpr;
+                for (int e = tid / cpr; e < W0; e += step) put(e, k);
+            } else {
+                for (int c = tid; c < W0 * cpr; c += nt) put(c / cpr, c % cpr);
+            }
+        }
         fence_proxy_async_shared();  // the rows are read by bulk stores (async proxy) below
         __syncthreads();
         // stash: raw rows of operand 0 straight from shared memory
-        if (stash != nullptr) {
+        if (stash != nullptr && compact == nullptr) {
             if (stash_bulk) {
                 if (a.n_slices == 1) {
                     if (tid == 0) {
@@ -192,8 +221,12 @@ __global__ void __launch_bounds__(kMaxThreads) gather_kernel(const GatherArgs a,
             const int64_t sl = slot[e];
             rows[(size_t)e * sw + j] = sl >= 0 ? __ldg(bank + sl * hd + c0 + j) : E(0);
         }
-        if (stash != nullptr)
+        if (compact != nullptr) {
+            for (int n = 0; n < W0; ++n)
+                if (kp[n] >= 0) compact[(int64_t)kp[n] * hd + c0 + j] = rows[(size_t)n * sw + j];
+        } else if (stash != nullptr) {
             for (int n = 0; n < W0; ++n) stash[(t * W0 + n) * hd + c0 + j] = rows[(size_t)n * sw + j];
+        }
     }
 
     // weighted sums, one fmaf chain per column over ascending entries
@@ -246,7 +279,10 @@ int launch_gather(const GatherArgs& a0, int bank_dtype, int idx_dtype, int w_dty
     GatherArgs a = a0;
     if (a.tokens == 0) return 0;
     const int es = bank_dtype == SDM_BF16 ? 2 : 4;
-    const bool bulk = ((int64_t)a.hd * es) % 16 == 0 && reinterpret_cast<uintptr_t>(a.bank) % 16 == 0;
+    // 16-byte row pieces: whole rows of 16-byte multiples, an aligned bank, and for a compact
+    // snapshot (stored piece by piece) an aligned snapshot
+    const bool bulk = ((int64_t)a.hd * es) % 16 == 0 && reinterpret_cast<uintptr_t>(a.bank) % 16 == 0 &&
+                      (a.kpos == nullptr || reinterpret_cast<uintptr_t>(a.stash) % 16 == 0);
     const int cpt = (bulk && es == 2) ? 2 : 1;
     const int n_rows = a.width[0] + (a.n_ops == 2 ? a.width[1] : 0);
 
@@ -257,7 +293,8 @@ int launch_gather(const GatherArgs& a0, int bank_dtype, int idx_dtype, int w_dty
     a.n_slices = (a.hd + sw - 1) / sw;
     const int64_t blocks = a.tokens * a.n_slices;
     if (blocks > INT_MAX) return SDM_ECOUNT;
-    const int stash_bulk = a.stash != nullptr && reinterpret_cast<uintptr_t>(a.stash) % 16 == 0 && bulk;
+    const int stash_bulk =
+        a.stash != nullptr && a.kpos == nullptr && reinterpret_cast<uintptr_t>(a.stash) % 16 == 0 && bulk;
     const int threads = ((sw + cpt - 1) / cpt + 31) / 32 * 32;
     const size_t smem = GatherLayout(n_rows, sw, es).total;
     const dim3 grid((unsigned)blocks), block((unsigned)threads);

@@ -94,9 +94,16 @@ int sdm_decode_step(void* bank, const void* k_idx, const float* k_val, const flo
                           idx_dtype, stream);
 }
 
-int sdm_gather(const void* bank, int64_t n_slots, int hd, int bank_dtype, int n_ops, const void* const idx[2],
-               const void* const w[2], float* const out[2], const int width[2], int idx_dtype, int w_dtype,
-               void* stash, int64_t tokens, int chunk, int valid, const int32_t* chunk_valid, sdm_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// Shared validation and launch of the two gather entry points; `stash` is the stash, or the
+// compact snapshot when kpos is set (same byte size: tokens * width[0] rows).
+int gather_common(const void* bank, int64_t n_slots, int hd, int bank_dtype, int n_ops, const void* const idx[2],
+                  const void* const w[2], float* const out[2], const int width[2], int idx_dtype, int w_dtype,
+                  void* stash, const int32_t* kpos, bool compact, int64_t tokens, int chunk, int valid,
+                  const int32_t* chunk_valid, sdm_stream_t stream) {
     if (bank_dtype != SDM_BF16 && bank_dtype != SDM_F32) return SDM_EDTYPE;
     if (w_dtype != SDM_BF16 && w_dtype != SDM_F32) return SDM_EDTYPE;
     if (idx_dtype != SDM_I32 && idx_dtype != SDM_I64) return SDM_EIDX;
@@ -110,11 +117,13 @@ int sdm_gather(const void* bank, int64_t n_slots, int hd, int bank_dtype, int n_
     if (chunk_valid == nullptr && (valid < 0 || valid > chunk)) return SDM_ECHUNK;
     if (tokens == 0) return SDM_OK;
     if (!bank) return SDM_ENULL;
+    if (compact && (!stash || !kpos)) return SDM_ENULL;
     for (int o = 0; o < n_ops; ++o)
         if (!idx[o] || !w[o] || !out[o]) return SDM_ENULL;
     const size_t es = bank_dtype == SDM_BF16 ? 2 : 4, is = idx_dtype == SDM_I64 ? 8 : 4,
                  ws = w_dtype == SDM_BF16 ? 2 : 4;
-    if (!aligned(bank, es) || (stash && !aligned(stash, es)) || (chunk_valid && !aligned(chunk_valid, 4)))
+    if (!aligned(bank, es) || (stash && !aligned(stash, es)) || (chunk_valid && !aligned(chunk_valid, 4)) ||
+        (kpos && !aligned(kpos, 4)))
         return SDM_EALIGN;
     for (int o = 0; o < n_ops; ++o)
         if (!aligned(idx[o], is) || !aligned(w[o], ws) || !aligned(out[o], 4)) return SDM_EALIGN;
@@ -135,11 +144,31 @@ int sdm_gather(const void* bank, int64_t n_slots, int hd, int bank_dtype, int n_
         a.width[o] = width[o];
     }
     a.stash = stash;
+    a.kpos = compact ? kpos : nullptr;
     a.tokens = tokens;
     a.chunk = chunk;
     a.valid = valid;
     a.chunk_valid = chunk_valid;
     return sdm::launch_gather(a, bank_dtype, idx_dtype, w_dtype, reinterpret_cast<cudaStream_t>(stream));
+}
+
+}  // namespace
+
+extern "C" {
+
+int sdm_gather(const void* bank, int64_t n_slots, int hd, int bank_dtype, int n_ops, const void* const idx[2],
+               const void* const w[2], float* const out[2], const int width[2], int idx_dtype, int w_dtype,
+               void* stash, int64_t tokens, int chunk, int valid, const int32_t* chunk_valid, sdm_stream_t stream) {
+    return gather_common(bank, n_slots, hd, bank_dtype, n_ops, idx, w, out, width, idx_dtype, w_dtype, stash,
+                         nullptr, false, tokens, chunk, valid, chunk_valid, stream);
+}
+
+int sdm_gather_kpos(const void* bank, int64_t n_slots, int hd, int bank_dtype, int n_ops, const void* const idx[2],
+                    const void* const w[2], float* const out[2], const int width[2], int idx_dtype, int w_dtype,
+                    void* compact, const int32_t* kpos, int64_t tokens, int chunk, int valid,
+                    const int32_t* chunk_valid, sdm_stream_t stream) {
+    return gather_common(bank, n_slots, hd, bank_dtype, n_ops, idx, w, out, width, idx_dtype, w_dtype, compact,
+                         kpos, true, tokens, chunk, valid, chunk_valid, stream);
 }
 
 const char* sdm_status_string(int status) {

@@ -32,7 +32,8 @@ struct GatherArgs {
     const void* w[2];
     float* out[2];
     int width[2];
-    void* stash;
+    void* stash;             // [tokens, width[0], hd], or the compact snapshot when kpos is set
+    const int32_t* kpos;     // [tokens, width[0]] compact-snapshot rows (-1: none), or nullptr
     int64_t tokens;
     int chunk, valid;
     const int32_t* chunk_valid;

@@ -20,8 +20,8 @@ SDM_BF16, SDM_F32 = 0, 1
 SDM_I32, SDM_I64 = 0, 1
 SDM_DEV_TIMEOUT, SDM_DEV_BAD_INDEX = 1, 2
 
-ENTRY_POINTS = ("sdm_decode_step", "sdm_decode_seq", "sdm_gather", "sdm_status_string", "sdm_device_status",
-                "sdm_version")
+ENTRY_POINTS = ("sdm_decode_step", "sdm_decode_seq", "sdm_gather", "sdm_gather_kpos", "sdm_status_string",
+                "sdm_device_status", "sdm_version")
 
 _BANK_CODES = {torch.bfloat16: SDM_BF16, torch.float32: SDM_F32}
 _IDX_CODES = {torch.int32: SDM_I32, torch.int64: SDM_I64}
@@ -58,6 +58,10 @@ def library() -> ctypes.CDLL:
             lib.sdm_gather.argtypes = [vp, i64, i32, i32, i32, ctypes.POINTER(vp), ctypes.POINTER(vp),
                                        ctypes.POINTER(vp), ctypes.POINTER(i32), i32, i32, vp, i64, i32, i32, vp, vp]
             lib.sdm_gather.restype = i32
+            lib.sdm_gather_kpos.argtypes = [vp, i64, i32, i32, i32, ctypes.POINTER(vp), ctypes.POINTER(vp),
+                                            ctypes.POINTER(vp), ctypes.POINTER(i32), i32, i32, vp, vp, i64, i32, i32,
+                                            vp, vp]
+            lib.sdm_gather_kpos.restype = i32
             lib.sdm_status_string.argtypes = [i32]
             lib.sdm_status_string.restype = ctypes.c_char_p
             lib.sdm_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint), i32]
@@ -151,13 +155,17 @@ def decode_seq(bank, k_idx, k_val, v, beta, g, q_idx, q_val, out=None, stream=No
 
 
 def gather(bank, ops, *, chunk: int, valid: int | None = None, chunk_valid=None, stash=None, with_stash=True,
-           outs=None, stream=None):
+           outs=None, kpos=None, compact=None, stream=None):
     """Token gather (sdm_gather) with one or two operands ``ops = [(idx, w), ...]``.
 
     idx [tokens, width] int32/int64, w [tokens, width] bf16/float32. Returns (outs, stash):
     outs is a list of [tokens, hd] float32 tensors; stash [tokens, width0, hd] in the bank dtype
     (allocated when ``with_stash`` and not given), or None. ``valid`` is the scalar count
     (default: chunk) unless ``chunk_valid`` [tokens / chunk] int32 gives one per chunk.
+
+    With ``kpos`` [tokens, width0] int32 the call is sdm_gather_kpos: operand 0's rows go to the
+    compact snapshot ``compact`` [tokens / chunk, chunk * width0, hd] (written in place; only the
+    rows kpos names), which is returned in place of the stash.
     """
     if bank.dtype not in _BANK_CODES or bank.dim() != 2:
         raise TypeError("bank must be a [n_slots, head_dim] bfloat16 or float32 tensor")
@@ -183,6 +191,19 @@ def gather(bank, ops, *, chunk: int, valid: int | None = None, chunk_valid=None,
         _need(out, f"out[{o}]", dev)
         _f32(out, f"out[{o}]")
         _shape(out, f"out[{o}]", (tokens, hd))
+    if kpos is not None:
+        _need(kpos, "kpos", dev)
+        if kpos.dtype != torch.int32:
+            raise TypeError("kpos must be int32")
+        _shape(kpos, "kpos", tuple(ops[0][0].shape))
+        if compact is None:
+            raise ValueError("kpos needs the compact snapshot tensor")
+        _need(compact, "compact", dev)
+        if compact.dtype != bank.dtype:
+            raise TypeError("compact must have the bank dtype")
+        if tokens % chunk == 0:
+            _shape(compact, "compact", (tokens // chunk, chunk * ops[0][0].shape[1], hd))
+        stash, with_stash = None, False
     if stash is None and with_stash:
         stash = torch.empty((tokens, ops[0][0].shape[1], hd), dtype=bank.dtype, device=dev)
     if stash is not None:
@@ -204,10 +225,16 @@ def gather(bank, ops, *, chunk: int, valid: int | None = None, chunk_valid=None,
     w_arr = (vp * 2)(*[vp(op[1].data_ptr()) for op in ops], *([vp(0)] * (2 - n)))
     out_arr = (vp * 2)(*[vp(o.data_ptr()) for o in outs], *([vp(0)] * (2 - n)))
     width_arr = (ctypes.c_int * 2)(*[op[0].shape[1] for op in ops], *([0] * (2 - n)))
+    cv_ptr = chunk_valid.data_ptr() if chunk_valid is not None else None
+    if kpos is not None:
+        rc = library().sdm_gather_kpos(bank.data_ptr(), n_slots, hd, _BANK_CODES[bank.dtype], n, idx_arr, w_arr,
+                                       out_arr, width_arr, _IDX_CODES[idx_dt], _BANK_CODES[w_dt], compact.data_ptr(),
+                                       kpos.data_ptr(), tokens, chunk, valid, cv_ptr, _stream_handle(stream, dev))
+        _check("sdm_gather_kpos", rc)
+        return outs, compact
     rc = library().sdm_gather(bank.data_ptr(), n_slots, hd, _BANK_CODES[bank.dtype], n, idx_arr, w_arr, out_arr,
                               width_arr, _IDX_CODES[idx_dt], _BANK_CODES[w_dt],
-                              stash.data_ptr() if stash is not None else None, tokens, chunk, valid,
-                              chunk_valid.data_ptr() if chunk_valid is not None else None,
+                              stash.data_ptr() if stash is not None else None, tokens, chunk, valid, cv_ptr,
                               _stream_handle(stream, dev))
     _check("sdm_gather", rc)
     return outs, stash

@@ -135,6 +135,27 @@ int sdm_gather(const void* bank, int64_t n_slots, int hd, int bank_dtype, int n_
                const void* const w[2], float* const out[2], const int width[2], int idx_dtype, int w_dtype,
                void* stash, int64_t tokens, int chunk, int valid, const int32_t* chunk_valid, sdm_stream_t stream);
 
+/*
+ * sdm_gather_kpos - token gather with a compact snapshot of operand 0 instead of the stash
+ * (gather_cuda.py, the compact-snapshot form of the kernel: `kpos`, `crow`).
+ *
+ * Outputs as sdm_gather. Operand 0's rows go to a snapshot of chunk * width[0] rows per chunk:
+ * for every live token t and entry n with kpos[t, n] >= 0,
+ *     compact[t / chunk, kpos[t, n], :] = bank[idx[0][t, n], :]
+ * (kpos names the entry's first position among the chunk's sorted rows, so each distinct row is
+ * stored once per chunk). Entries with kpos = -1 and padding tokens store nothing, and no other
+ * snapshot row is written. An entry whose kpos is >= chunk * width[0] or whose row index is outside
+ * [0, n_slots) stores nothing and raises SDM_DEV_BAD_INDEX.
+ *
+ *   compact    [tokens / chunk, chunk * width[0], hd] bank dtype (device), must not overlap the bank
+ *   kpos       [tokens, width[0]] int32 (device)
+ * Other arguments as sdm_gather (there is no stash argument).
+ */
+int sdm_gather_kpos(const void* bank, int64_t n_slots, int hd, int bank_dtype, int n_ops, const void* const idx[2],
+                    const void* const w[2], float* const out[2], const int width[2], int idx_dtype, int w_dtype,
+                    void* compact, const int32_t* kpos, int64_t tokens, int chunk, int valid,
+                    const int32_t* chunk_valid, sdm_stream_t stream);
+
 /* A static string naming a return code of the calls above. */
 const char* sdm_status_string(int status);
 

@@ -135,3 +135,23 @@ def test_binding_rejects_host_tensors():
 def test_binding_rejects_bad_dtypes():
     with pytest.raises(TypeError):
         sdm.decode_step(torch.zeros((4, 4), dtype=torch.float16), *([torch.zeros(1)] * 7))
+
+
+def _gather_kpos(lib, **kw):
+    a = dict(bank=FAKE, n_slots=1000, hd=64, bank_dtype=0, n_ops=1, idx=(FAKE + (1 << 24), 0),
+             w=(FAKE + (3 << 24), 0), out=(FAKE + (5 << 24), 0), width=(8, 0), idx_dtype=1, w_dtype=0,
+             compact=FAKE + (8 << 24), kpos=FAKE + (9 << 24), tokens=64, chunk=16, valid=16, chunk_valid=None)
+    a.update(kw)
+    vp = ctypes.c_void_p
+    return lib.sdm_gather_kpos(a["bank"], a["n_slots"], a["hd"], a["bank_dtype"], a["n_ops"], (vp * 2)(*a["idx"]),
+                               (vp * 2)(*a["w"]), (vp * 2)(*a["out"]), (ctypes.c_int * 2)(*a["width"]),
+                               a["idx_dtype"], a["w_dtype"], a["compact"], a["kpos"], a["tokens"], a["chunk"],
+                               a["valid"], a["chunk_valid"], None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(compact=0), "SDM_ENULL"), (dict(kpos=0), "SDM_ENULL"), (dict(kpos=FAKE + (9 << 24) + 2), "SDM_EALIGN"),
+    (dict(compact=FAKE + 64), "SDM_EOVERLAP"), (dict(chunk=5), "SDM_ECHUNK"), (dict(width=(300, 0)), "SDM_EWIDTH"),
+])
+def test_gather_kpos_argument_errors(lib, kw, code):
+    assert _gather_kpos(lib, **kw) == CODES[code]

@@ -154,3 +154,99 @@ def test_gather_full_size():
     for o, (idx, w) in enumerate(g["ops"]):
         ref, _, _ = oracle.gather(bank_h, to_np(idx[sample]), to_np(w[sample]), chunk=1, stash=False)
         assert bits_equal(to_np(outs[o][sample]), ref)
+
+
+def _first_occurrence_kpos(idx: np.ndarray, chunk: int, live: np.ndarray) -> np.ndarray:
+    """kpos of each chunk's first occurrences: position in the chunk's sorted entries (numpy)."""
+    tokens, W0 = idx.shape
+    kpos = np.full((tokens, W0), -1, np.int32)
+    for c in range(tokens // chunk):
+        ent = idx[c * chunk:(c + 1) * chunk].ravel()
+        order = np.sort(ent)
+        _, first = np.unique(ent, return_index=True)
+        for e in first:
+            t = c * chunk + e // W0
+            kpos[t, e % W0] = int(np.searchsorted(order, ent[e]))
+    kpos[~live] = np.where(kpos[~live] >= 0, 0, -1)  # padding tokens name rows too; they must store nothing
+    return kpos
+
+
+KPOS_CASES = [
+    ("bf16", "bf16", "i64", 3000, 128, 128, 16, (32, 32)),
+    ("f32", "f32", "i32", 500, 520, 16, 4, (12,)),       # rows cut into slices
+    ("bf16", "f32", "i32", 300, 13, 24, 6, (5, 7)),       # 26-byte rows: plain-load path
+]
+
+
+@pytest.mark.parametrize("case", KPOS_CASES, ids=[f"{c[0]}-hd{c[4]}-{'x'.join(map(str, c[7]))}" for c in KPOS_CASES])
+def test_gather_kpos_matches_oracle(case):
+    bank_dt, w_dt, idx_dt, n_slots, hd, tokens, chunk, widths = case
+    wl = _gw(bank_dt, w_dt, idx_dt, n_slots, hd, tokens, chunk, widths, True, True, seed=21)
+    g = workloads.make_gather_inputs(wl, device=DEV)
+    idx0 = to_np(g["ops"][0][0])
+    live = (np.arange(tokens) % chunk) < np.repeat(to_np(g["chunk_valid"]), chunk)
+    kpos = _first_occurrence_kpos(idx0, chunk, live)
+    W0 = widths[0]
+    compact = torch.full((tokens // chunk, chunk * W0, hd), float("nan"), dtype=g["bank"].dtype, device=DEV)
+    ref_compact = to_np(compact)
+    outs, comp = sdm.gather(g["bank"], g["ops"], chunk=chunk, chunk_valid=g["chunk_valid"],
+                            kpos=torch.from_numpy(kpos).to(DEV), compact=compact)
+    torch.cuda.synchronize()
+    assert comp is compact
+    oracle.gather_kpos(to_np(g["bank"]), idx0, kpos, ref_compact, chunk=chunk, chunk_valid=to_np(g["chunk_valid"]))
+    assert bits_equal(to_np(compact), ref_compact)
+    r0, r1, _ = _oracle(g, wl)
+    assert bits_equal(to_np(outs[0]), r0)
+    if len(widths) == 2:
+        assert bits_equal(to_np(outs[1]), r1)
+    assert sdm.device_status() == 0
+
+
+def test_gather_kpos_out_of_range_is_skipped_and_flagged():
+    wl = _gw("bf16", "bf16", "i64", 800, 64, 16, 8, (4,), True, False, seed=22)
+    g = workloads.make_gather_inputs(wl, device=DEV)
+    kpos = torch.full((16, 4), -1, dtype=torch.int32, device=DEV)
+    kpos[0, 0] = 0
+    kpos[1, 2] = 8 * 4  # one past the chunk's snapshot
+    compact = torch.zeros((2, 32, 64), dtype=torch.bfloat16, device=DEV)
+    sdm.device_status(clear=True)
+    sdm.gather(g["bank"], g["ops"], chunk=8, kpos=kpos, compact=compact)
+    torch.cuda.synchronize()
+    assert sdm.device_status(clear=True) & sdm.SDM_DEV_BAD_INDEX
+    assert torch.equal(compact[0, 0], g["bank"][g["ops"][0][0][0, 0]])
+    assert not compact[0, 1:].view(torch.int16).any() and not compact[1].view(torch.int16).any()
+
+
+def test_gather_kpos_full_size():
+    """The full gather workload with a compact snapshot: every named row equals torch's own row
+    indexing, every other snapshot row keeps its sentinel bits, outputs equal the stash form's."""
+    wl = workloads.C4
+    g = workloads.make_gather_inputs(wl, device=DEV)
+    live = ((torch.arange(wl.tokens, device=DEV) % wl.chunk) < g["chunk_valid"].repeat_interleave(wl.chunk))
+    idx0 = g["ops"][0][0]
+    W0 = idx0.shape[1]
+    # first occurrence of each row within its chunk (torch on the GPU): sort each chunk's entries
+    ent = idx0.view(wl.tokens // wl.chunk, wl.chunk * W0)
+    srt, order = ent.sort(dim=1, stable=True)
+    first_sorted = torch.ones_like(srt, dtype=torch.bool)
+    first_sorted[:, 1:] = srt[:, 1:] != srt[:, :-1]
+    pos = torch.arange(srt.shape[1], device=DEV).expand_as(srt)
+    first_pos = torch.cummax(torch.where(first_sorted, pos, torch.zeros_like(pos)), dim=1).values
+    kp_sorted = torch.where(first_sorted, first_pos, torch.full_like(first_pos, -1))
+    kpos = torch.empty_like(kp_sorted).scatter_(1, order, kp_sorted).view(wl.tokens, W0).to(torch.int32)
+    compact = torch.full((wl.tokens // wl.chunk, wl.chunk * W0, wl.hd), float("nan"), dtype=torch.bfloat16, device=DEV)
+    sentinel = compact[0, 0].clone()
+    outs, _ = sdm.gather(g["bank"], g["ops"], chunk=wl.chunk, chunk_valid=g["chunk_valid"], kpos=kpos,
+                         compact=compact)
+    outs_ref, _ = sdm.gather(g["bank"], g["ops"], chunk=wl.chunk, chunk_valid=g["chunk_valid"], with_stash=False)
+    torch.cuda.synchronize()
+    named = (kpos >= 0) & live[:, None]
+    t_idx, n_idx = torch.nonzero(named, as_tuple=True)
+    rows = compact[t_idx // wl.chunk, kpos[t_idx, n_idx].long()]
+    assert torch.equal(rows.view(torch.int16), g["bank"][idx0[t_idx, n_idx]].view(torch.int16))
+    mask = torch.zeros(compact.shape[:2], dtype=torch.bool, device=DEV)
+    mask[t_idx // wl.chunk, kpos[t_idx, n_idx].long()] = True
+    assert torch.equal(compact[~mask].view(torch.int16), sentinel.expand(int((~mask).sum()), -1).view(torch.int16))
+    for a, b in zip(outs, outs_ref):
+        assert torch.equal(a.view(torch.int32), b.view(torch.int32))
+    assert sdm.device_status() == 0
