@@ -1,0 +1,50 @@
+"""CUDA-graph templates for repeated decode launches.
+
+Every C-ABI call only enqueues work on the caller's stream and allocates nothing, so a sequence of
+them can be captured once and replayed. ``DecodeStepGraph`` captures T single-token
+``sdm_decode_step`` launches (one per token, each reading its own slab of fixed device input
+buffers) into one graph: fill ``inputs`` (device tensors, time-major [T, S, .]) and call
+``replay()``; the readings land in ``out`` [T, S, hd]. This replaces T separate host calls (and
+their per-call argument checks) by one graph launch; the kernels are the same.
+"""
+
+from __future__ import annotations
+
+import torch
+
+from . import sdm
+
+DECODE_INPUTS = ("k_idx", "k_val", "v", "beta", "g", "q_idx", "q_val")
+
+
+class DecodeStepGraph:
+    """T single-token decode steps of ``bank`` captured in one CUDA graph."""
+
+    def __init__(self, bank: torch.Tensor, like: dict, warmup: bool = True):
+        dev = bank.device
+        self.bank = bank
+        self.inputs = {k: torch.zeros(like[k].shape, dtype=like[k].dtype, device=dev) for k in DECODE_INPUTS}
+        T, S = like["k_idx"].shape[:2]
+        self.T = T
+        self.out = torch.empty((T, S, bank.shape[1]), dtype=bank.dtype, device=dev)
+        self.graph = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(torch.cuda.current_stream(dev))
+        with torch.cuda.stream(side):
+            if warmup:  # first calls outside capture (library load, attribute queries)
+                saved = bank.clone()
+                self._steps()
+                bank.copy_(saved)
+                torch.cuda.current_stream(dev).synchronize()
+            with torch.cuda.graph(self.graph, stream=side):
+                self._steps()
+        torch.cuda.current_stream(dev).wait_stream(side)
+
+    def _steps(self):
+        for t in range(self.T):
+            sdm.decode_step(self.bank, *(self.inputs[k][t] for k in DECODE_INPUTS), out=self.out[t])
+
+    def replay(self) -> torch.Tensor:
+        """Run the T captured steps on the current contents of ``inputs``; returns ``out``."""
+        self.graph.replay()
+        return self.out
