@@ -28,11 +28,6 @@ __device__ __forceinline__ float from_f32<float>(float x) { return x; }
 template <typename E>
 __device__ __forceinline__ float round_to(float x) { return to_f32(from_f32<E>(x)); }
 
-// two bf16 values packed little-endian (lo in bits 0-15)
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
-    return uint32_t(from_f32<uint16_t>(lo)) | (uint32_t(from_f32<uint16_t>(hi)) << 16);
-}
-
 template <typename I>
 __device__ __forceinline__ int64_t load_index(const void* p, int64_t i) {
     return (int64_t)__ldg(static_cast<const I*>(p) + i);
