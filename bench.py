@@ -270,10 +270,11 @@ class Case:
         wl = self.wl
         par = f"weak: {r.world} independent shard(s), no collective in the data path"
         if self.kind == "gather":
+            gib = wl.n_slots * wl.hd * (2 if wl.bank_dtype == "bf16" else 4) / 2 ** 30
             return {"workload": wl.name, "n_slots": wl.n_slots, "head_dim": wl.hd, "tokens": wl.tokens,
                     "chunk": wl.chunk, "widths": list(wl.widths), "bank_dtype": wl.bank_dtype,
                     "idx_dtype": wl.idx_dtype, "w_dtype": wl.w_dtype, "stash": wl.stash, "call": "sdm_gather",
-                    "l2": "inputs larger than L2 (1 GiB bank), no flush", "parallelism": par}
+                    "l2": f"inputs larger than L2 ({gib:.0f} GiB bank), no flush", "parallelism": par}
         bank_gib = wl.n_slots * wl.hd * (2 if wl.bank_dtype == "bf16" else 4) / 2 ** 30
         return {"workload": wl.name, "streams": wl.n_streams, "head_dim": wl.hd,
                 "slots_per_stream": wl.slots_per_stream, "W": wl.W, "R": wl.R, "G": wl.G, "T": wl.T,
@@ -486,6 +487,39 @@ def extras(args, dev, r: sdist.Rank, peak: float, skip: str):
     return res
 
 
+def plan_slabs(dev, slab: int = 256) -> dict:
+    """The gather workload's index tensor walked in slabs of `slab` tokens: one launch per slab
+    through a gather plan (checked once) against direct sdm_gather calls on the same slabs (no
+    stash). Device time per walk and host time per call, for the launch-overhead comparison."""
+    from decode_state_gb300 import sdm
+
+    wl = workloads.C4.scaled(stash=False, per_chunk_valid=False)
+    g = workloads.make_gather_inputs(wl, device=dev)
+    n = wl.tokens // slab
+    plan = sdm.GatherPlan(g["bank"], g["ops"], tokens=slab, chunk=wl.chunk)
+    outs = plan.outs
+    slabs = [[(i[k * slab:(k + 1) * slab], w[k * slab:(k + 1) * slab]) for i, w in g["ops"]] for k in range(n)]
+
+    def via_plan():
+        for k in range(n):
+            plan.launch(k * slab)
+
+    def direct():
+        for k in range(n):
+            sdm.gather(g["bank"], slabs[k], chunk=wl.chunk, outs=outs, with_stash=False)
+
+    res = {"slab_tokens": slab, "launches_per_walk": n}
+    for name, fn in (("plan", via_plan), ("direct", direct)):
+        ms = _time_calls(fn, 5)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        fn()
+        host_us = (time.perf_counter() - t0) * 1e6 / n
+        torch.cuda.synchronize()
+        res[name] = {"ms_per_walk": ms, "us_per_launch": ms * 1e3 / n, "host_us_per_call": host_us}
+    return res
+
+
 # ---------------------------------------------------------------- reference arm (the oracle)
 
 
@@ -547,6 +581,8 @@ def main():
         if r.is_root and r.world == 1 and not args.no_extras:
             res["other_workloads"] = extras(args, torch.device("cuda", r.local_rank), r, res["roofline"]["peak"],
                                             res["config"]["workload"])
+            res["other_workloads"]["gather_plan_slabs"] = plan_slabs(torch.device("cuda", r.local_rank))
+            torch.cuda.empty_cache()
         if r.is_root:
             print(json.dumps(res), flush=True)
     finally:

@@ -253,18 +253,17 @@ __global__ void __launch_bounds__(kMaxThreads) gather_kernel(const GatherArgs a,
 }
 
 template <typename E, typename I, typename WT>
-int launch_typed(bool bulk, const GatherArgs& a, int stash_bulk, dim3 grid, dim3 block, size_t smem,
-                 cudaStream_t stream) {
+void resolve_typed(bool bulk, GatherLaunch* L) {
     const auto kernel = bulk ? gather_kernel<E, I, WT, true> : gather_kernel<E, I, WT, false>;
-    const int early = fits_one_wave(kernel, grid.x, (int)block.x, smem) ? 1 : 0;
-    return launch_pdl(kernel, grid, block, smem, stream, a, stash_bulk, early);
+    L->fn = reinterpret_cast<const void*>(kernel);
 }
 
 template <typename E, typename I>
-int launch_w(int w_dtype, bool bulk, const GatherArgs& a, int stash_bulk, dim3 grid, dim3 block, size_t smem,
-             cudaStream_t stream) {
-    return w_dtype == SDM_BF16 ? launch_typed<E, I, uint16_t>(bulk, a, stash_bulk, grid, block, smem, stream)
-                               : launch_typed<E, I, float>(bulk, a, stash_bulk, grid, block, smem, stream);
+void resolve_w(int w_dtype, bool bulk, GatherLaunch* L) {
+    if (w_dtype == SDM_BF16)
+        resolve_typed<E, I, uint16_t>(bulk, L);
+    else
+        resolve_typed<E, I, float>(bulk, L);
 }
 
 int shrink_cols(int sw, bool bulk, int es) {
@@ -275,8 +274,10 @@ int shrink_cols(int sw, bool bulk, int es) {
 
 }  // namespace
 
-int launch_gather(const GatherArgs& a0, int bank_dtype, int idx_dtype, int w_dtype, cudaStream_t stream) {
-    GatherArgs a = a0;
+int plan_gather(const GatherArgs& a0, int bank_dtype, int idx_dtype, int w_dtype, GatherLaunch* L) {
+    *L = GatherLaunch{};
+    L->a = a0;
+    GatherArgs& a = L->a;
     if (a.tokens == 0) return 0;
     const int es = bank_dtype == SDM_BF16 ? 2 : 4;
     // 16-byte row pieces: whole rows of 16-byte multiples, an aligned bank, and for a compact
@@ -293,17 +294,46 @@ int launch_gather(const GatherArgs& a0, int bank_dtype, int idx_dtype, int w_dty
     a.n_slices = (a.hd + sw - 1) / sw;
     const int64_t blocks = a.tokens * a.n_slices;
     if (blocks > INT_MAX) return SDM_ECOUNT;
-    const int stash_bulk =
+    L->stash_bulk =
         a.stash != nullptr && a.kpos == nullptr && reinterpret_cast<uintptr_t>(a.stash) % 16 == 0 && bulk;
-    const int threads = ((sw + cpt - 1) / cpt + 31) / 32 * 32;
-    const size_t smem = GatherLayout(n_rows, sw, es).total;
-    const dim3 grid((unsigned)blocks), block((unsigned)threads);
+    L->grid = (unsigned)blocks;
+    L->block = (unsigned)(((sw + cpt - 1) / cpt + 31) / 32 * 32);
+    L->smem = GatherLayout(n_rows, sw, es).total;
     if (bank_dtype == SDM_BF16) {
-        return idx_dtype == SDM_I32 ? launch_w<uint16_t, int32_t>(w_dtype, bulk, a, stash_bulk, grid, block, smem, stream)
-                                    : launch_w<uint16_t, int64_t>(w_dtype, bulk, a, stash_bulk, grid, block, smem, stream);
+        if (idx_dtype == SDM_I32)
+            resolve_w<uint16_t, int32_t>(w_dtype, bulk, L);
+        else
+            resolve_w<uint16_t, int64_t>(w_dtype, bulk, L);
+    } else {
+        if (idx_dtype == SDM_I32)
+            resolve_w<float, int32_t>(w_dtype, bulk, L);
+        else
+            resolve_w<float, int64_t>(w_dtype, bulk, L);
     }
-    return idx_dtype == SDM_I32 ? launch_w<float, int32_t>(w_dtype, bulk, a, stash_bulk, grid, block, smem, stream)
-                                : launch_w<float, int64_t>(w_dtype, bulk, a, stash_bulk, grid, block, smem, stream);
+    // the early trigger only when every block of this launch is resident at once
+    int per_sm = 0;
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, L->fn, (int)L->block, L->smem);
+    if (e != cudaSuccess) {
+        (void)cudaGetLastError();
+        per_sm = 0;
+    }
+    L->early_trigger = blocks <= (int64_t)per_sm * sm_count() ? 1 : 0;
+    return 0;
+}
+
+int run_gather(const GatherLaunch& L, cudaStream_t stream) {
+    if (L.fn == nullptr) return 0;
+    GatherArgs a = L.a;
+    int stash_bulk = L.stash_bulk, early = L.early_trigger;
+    void* args[] = {&a, &stash_bulk, &early};
+    return launch_pdl_raw(L.fn, dim3(L.grid), dim3(L.block), L.smem, stream, args);
+}
+
+int launch_gather(const GatherArgs& a, int bank_dtype, int idx_dtype, int w_dtype, cudaStream_t stream) {
+    GatherLaunch L;
+    const int rc = plan_gather(a, bank_dtype, idx_dtype, w_dtype, &L);
+    if (rc != 0) return rc;
+    return run_gather(L, stream);
 }
 
 int gather_status(unsigned int* word, bool clear) {

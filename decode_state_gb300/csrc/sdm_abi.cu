@@ -3,6 +3,7 @@
 // > 0 = cudaError_t.
 #include <atomic>
 #include <climits>
+#include <cstring>
 
 #include "sdm.h"
 #include "sdm_internal.h"
@@ -98,12 +99,13 @@ int sdm_decode_step(void* bank, const void* k_idx, const float* k_val, const flo
 
 namespace {
 
-// Shared validation and launch of the two gather entry points; `stash` is the stash, or the
-// compact snapshot when kpos is set (same byte size: tokens * width[0] rows).
-int gather_common(const void* bank, int64_t n_slots, int hd, int bank_dtype, int n_ops, const void* const idx[2],
-                  const void* const w[2], float* const out[2], const int width[2], int idx_dtype, int w_dtype,
-                  void* stash, const int32_t* kpos, bool compact, int64_t tokens, int chunk, int valid,
-                  const int32_t* chunk_valid, sdm_stream_t stream) {
+// Shared validation of the gather entry points; fills *a when the arguments pass (SDM_OK). `stash`
+// is the stash, or the compact snapshot when kpos is set (same byte size: tokens * width[0] rows).
+int check_gather(const void* bank, int64_t n_slots, int hd, int bank_dtype, int n_ops, const void* const idx[2],
+                 const void* const w[2], float* const out[2], const int width[2], int idx_dtype, int w_dtype,
+                 void* stash, const int32_t* kpos, bool compact, int64_t tokens, int chunk, int valid,
+                 const int32_t* chunk_valid, sdm::GatherArgs* a) {
+    *a = sdm::GatherArgs{};
     if (bank_dtype != SDM_BF16 && bank_dtype != SDM_F32) return SDM_EDTYPE;
     if (w_dtype != SDM_BF16 && w_dtype != SDM_F32) return SDM_EDTYPE;
     if (idx_dtype != SDM_I32 && idx_dtype != SDM_I64) return SDM_EIDX;
@@ -115,7 +117,10 @@ int gather_common(const void* bank, int64_t n_slots, int hd, int bank_dtype, int
     if (n_slots < 1 || n_slots > (int64_t)INT_MAX || tokens < 0 || tokens > (int64_t)INT_MAX) return SDM_ECOUNT;
     if (chunk < 1 || tokens % chunk != 0) return SDM_ECHUNK;
     if (chunk_valid == nullptr && (valid < 0 || valid > chunk)) return SDM_ECHUNK;
-    if (tokens == 0) return SDM_OK;
+    if (tokens == 0) {
+        a->chunk = chunk;
+        return SDM_OK;
+    }
     if (!bank) return SDM_ENULL;
     if (compact && (!stash || !kpos)) return SDM_ENULL;
     for (int o = 0; o < n_ops; ++o)
@@ -132,24 +137,50 @@ int gather_common(const void* bank, int64_t n_slots, int hd, int bank_dtype, int
         if (overlaps(out[o], (size_t)tokens * hd * 4, bank, bank_bytes)) return SDM_EOVERLAP;
     if (stash && overlaps(stash, (size_t)tokens * width[0] * hd * es, bank, bank_bytes)) return SDM_EOVERLAP;
 
-    sdm::GatherArgs a{};
-    a.bank = bank;
-    a.n_slots = n_slots;
-    a.hd = hd;
-    a.n_ops = n_ops;
+    a->bank = bank;
+    a->n_slots = n_slots;
+    a->hd = hd;
+    a->n_ops = n_ops;
     for (int o = 0; o < n_ops; ++o) {
-        a.idx[o] = idx[o];
-        a.w[o] = w[o];
-        a.out[o] = out[o];
-        a.width[o] = width[o];
+        a->idx[o] = idx[o];
+        a->w[o] = w[o];
+        a->out[o] = out[o];
+        a->width[o] = width[o];
     }
-    a.stash = stash;
-    a.kpos = compact ? kpos : nullptr;
-    a.tokens = tokens;
-    a.chunk = chunk;
-    a.valid = valid;
-    a.chunk_valid = chunk_valid;
+    a->stash = stash;
+    a->kpos = compact ? kpos : nullptr;
+    a->tokens = tokens;
+    a->chunk = chunk;
+    a->valid = valid;
+    a->chunk_valid = chunk_valid;
+    return SDM_OK;
+}
+
+int gather_common(const void* bank, int64_t n_slots, int hd, int bank_dtype, int n_ops, const void* const idx[2],
+                  const void* const w[2], float* const out[2], const int width[2], int idx_dtype, int w_dtype,
+                  void* stash, const int32_t* kpos, bool compact, int64_t tokens, int chunk, int valid,
+                  const int32_t* chunk_valid, sdm_stream_t stream) {
+    sdm::GatherArgs a;
+    const int rc = check_gather(bank, n_slots, hd, bank_dtype, n_ops, idx, w, out, width, idx_dtype, w_dtype, stash,
+                                kpos, compact, tokens, chunk, valid, chunk_valid, &a);
+    if (rc != SDM_OK || tokens == 0) return rc;
     return sdm::launch_gather(a, bank_dtype, idx_dtype, w_dtype, reinterpret_cast<cudaStream_t>(stream));
+}
+
+// The contents of an sdm_gather_plan record. The tag mixes in an address inside this library, so a
+// record made by another load of the library (whose kernel addresses differ) is refused.
+struct PlanRecord {
+    uint64_t tag;
+    uint64_t bytes;
+    int64_t row0_max;
+    int64_t idx_row_bytes[2], w_row_bytes[2];  // bytes per index / weight row of each operand
+    int32_t device, chunk;
+    sdm::GatherLaunch launch;  // the launch at row0 = 0, valid = chunk
+};
+static_assert(sizeof(PlanRecord) <= SDM_GATHER_PLAN_BYTES, "gather plan record too large");
+
+uint64_t plan_tag() {
+    return 0x4e414c5047534453ull ^ (uint64_t)reinterpret_cast<uintptr_t>(&check_gather);
 }
 
 }  // namespace
@@ -171,6 +202,65 @@ int sdm_gather_kpos(const void* bank, int64_t n_slots, int hd, int bank_dtype, i
                          kpos, true, tokens, chunk, valid, chunk_valid, stream);
 }
 
+int sdm_gather_plan_init(sdm_gather_plan* plan, const void* bank, int64_t n_slots, int hd, int bank_dtype, int n_ops,
+                         const void* const idx[2], const void* const w[2], float* const out[2], const int width[2],
+                         int idx_dtype, int w_dtype, int64_t rows, int64_t row0_max, int64_t tokens, int chunk) {
+    if (!plan) return SDM_ENULL;
+    sdm::GatherArgs a;
+    int rc = check_gather(bank, n_slots, hd, bank_dtype, n_ops, idx, w, out, width, idx_dtype, w_dtype, nullptr,
+                          nullptr, false, tokens, chunk, chunk, nullptr, &a);
+    if (rc != SDM_OK) return rc;
+    if (row0_max < 0 || rows < tokens || row0_max > rows - tokens) return SDM_EROW;
+    PlanRecord p{};
+    const int64_t is = idx_dtype == SDM_I64 ? 8 : 4, ws = w_dtype == SDM_BF16 ? 2 : 4;
+    for (int o = 0; o < n_ops; ++o) {
+        p.idx_row_bytes[o] = is * width[o];
+        p.w_row_bytes[o] = ws * width[o];
+    }
+    p.row0_max = row0_max;
+    p.chunk = chunk;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) {
+        (void)cudaGetLastError();
+        return (int)e;
+    }
+    p.device = dev;
+    if (tokens > 0) {
+        rc = sdm::plan_gather(a, bank_dtype, idx_dtype, w_dtype, &p.launch);
+        if (rc != 0) return rc;
+    }
+    p.tag = plan_tag();
+    p.bytes = sizeof(PlanRecord);
+    static_assert(sizeof(sdm_gather_plan) == SDM_GATHER_PLAN_BYTES, "plan record size");
+    std::memset(plan, 0, sizeof(sdm_gather_plan));
+    std::memcpy(plan, &p, sizeof(p));
+    return SDM_OK;
+}
+
+int sdm_gather_plan_launch(const sdm_gather_plan* plan, int64_t row0, int valid, sdm_stream_t stream) {
+    if (!plan) return SDM_ENULL;
+    PlanRecord p;
+    std::memcpy(&p, plan, sizeof(p));
+    if (p.tag != plan_tag() || p.bytes != sizeof(PlanRecord)) return SDM_EPLAN;
+    if (row0 < 0 || row0 > p.row0_max) return SDM_EROW;
+    if (valid < 0 || valid > p.chunk) return SDM_ECHUNK;
+    if (p.launch.fn == nullptr) return SDM_OK;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return SDM_EDEVICE;
+    }
+    if (dev != p.device) return SDM_EDEVICE;
+    sdm::GatherArgs& a = p.launch.a;
+    for (int o = 0; o < a.n_ops; ++o) {
+        a.idx[o] = static_cast<const unsigned char*>(a.idx[o]) + row0 * p.idx_row_bytes[o];
+        a.w[o] = static_cast<const unsigned char*>(a.w[o]) + row0 * p.w_row_bytes[o];
+    }
+    a.valid = valid;
+    return sdm::run_gather(p.launch, reinterpret_cast<cudaStream_t>(stream));
+}
+
 const char* sdm_status_string(int status) {
     switch (status) {
         case SDM_OK: return "ok";
@@ -185,6 +275,9 @@ const char* sdm_status_string(int status) {
         case SDM_EALIGN: return "a pointer is not aligned to its element size";
         case SDM_EOVERLAP: return "a gather output or the stash overlaps the bank";
         case SDM_ENOPS: return "the gather takes one or two operands";
+        case SDM_EPLAN: return "not a gather plan made by sdm_gather_plan_init in this process";
+        case SDM_EROW: return "row0 outside 0..row0_max, or row0_max + tokens beyond the index rows";
+        case SDM_EDEVICE: return "the current device is not the gather plan's device";
         default: break;
     }
     if (status > 0) return cudaGetErrorString(static_cast<cudaError_t>(status));

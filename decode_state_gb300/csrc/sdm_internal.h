@@ -40,9 +40,21 @@ struct GatherArgs {
     int slice_cols, n_slices;
 };
 
+// A resolved gather launch: the kernel instance, its geometry and every kernel argument.
+struct GatherLaunch {
+    const void* fn;  // kernel (host stub of the template instance); nullptr: nothing to launch
+    GatherArgs a;
+    int stash_bulk, early_trigger;
+    unsigned int grid, block;
+    size_t smem;
+};
+
 // Validated launches (arguments already checked by the ABI layer). Return a cudaError_t.
 int launch_decode(const DecodeArgs& a, int bank_dtype, int idx_dtype, cudaStream_t stream);
 int launch_gather(const GatherArgs& a, int bank_dtype, int idx_dtype, int w_dtype, cudaStream_t stream);
+// launch_gather in two halves: choose the kernel and geometry (device queries, no launch), then launch.
+int plan_gather(const GatherArgs& a, int bank_dtype, int idx_dtype, int w_dtype, GatherLaunch* L);
+int run_gather(const GatherLaunch& L, cudaStream_t stream);
 
 // Device status words of the kernel files (OR of SDM_DEV_* bits); read and optionally reset.
 int decode_status(unsigned int* word, bool clear);
@@ -51,10 +63,10 @@ int gather_status(unsigned int* word, bool clear);
 // Multiprocessor count of the current device (cached per device).
 int sm_count();
 
-// Launch `kernel` with programmatic stream serialization (see grid_dependency_wait). Returns a
-// cudaError_t. Raises the dynamic shared-memory limit first when smem exceeds the default 48 KB.
-template <typename... P, typename... A>
-int launch_pdl(void (*kernel)(P...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream, A... args) {
+// Launch the kernel at address `kernel` (arguments as an array of pointers to them) with
+// programmatic stream serialization (see grid_dependency_wait). Returns a cudaError_t. Raises the
+// dynamic shared-memory limit first when smem exceeds the default 48 KB.
+inline int launch_pdl_raw(const void* kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t stream, void** args) {
     if (smem > 48 * 1024) {
         const cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) {
@@ -72,10 +84,23 @@ int launch_pdl(void (*kernel)(P...), dim3 grid, dim3 block, size_t smem, cudaStr
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, args...);
+    cudaError_t e = cudaLaunchKernelExC(&cfg, kernel, args);
     if (e == cudaSuccess) e = cudaGetLastError();
     else (void)cudaGetLastError();
     return (int)e;
+}
+
+template <typename T>
+struct Same {
+    using type = T;
+};
+
+// launch_pdl_raw for a typed kernel; the arguments are converted to the kernel's parameter types.
+template <typename... P>
+int launch_pdl(void (*kernel)(P...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+               typename Same<P>::type... args) {
+    void* argv[] = {&args...};
+    return launch_pdl_raw(reinterpret_cast<const void*>(kernel), grid, block, smem, stream, argv);
 }
 
 // True when all `blocks` of `kernel` can be resident at once, so that blocks of the next kernel

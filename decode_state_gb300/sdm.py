@@ -20,8 +20,9 @@ SDM_BF16, SDM_F32 = 0, 1
 SDM_I32, SDM_I64 = 0, 1
 SDM_DEV_TIMEOUT, SDM_DEV_BAD_INDEX = 1, 2
 
-ENTRY_POINTS = ("sdm_decode_step", "sdm_decode_seq", "sdm_gather", "sdm_gather_kpos", "sdm_status_string",
-                "sdm_device_status", "sdm_version")
+ENTRY_POINTS = ("sdm_decode_step", "sdm_decode_seq", "sdm_gather", "sdm_gather_kpos", "sdm_gather_plan_init",
+                "sdm_gather_plan_launch", "sdm_status_string", "sdm_device_status", "sdm_version")
+GATHER_PLAN_BYTES = 512  # SDM_GATHER_PLAN_BYTES
 
 _BANK_CODES = {torch.bfloat16: SDM_BF16, torch.float32: SDM_F32}
 _IDX_CODES = {torch.int32: SDM_I32, torch.int64: SDM_I64}
@@ -62,6 +63,11 @@ def library() -> ctypes.CDLL:
                                             ctypes.POINTER(vp), ctypes.POINTER(i32), i32, i32, vp, vp, i64, i32, i32,
                                             vp, vp]
             lib.sdm_gather_kpos.restype = i32
+            lib.sdm_gather_plan_init.argtypes = [vp, vp, i64, i32, i32, i32, ctypes.POINTER(vp), ctypes.POINTER(vp),
+                                                 ctypes.POINTER(vp), ctypes.POINTER(i32), i32, i32, i64, i64, i64, i32]
+            lib.sdm_gather_plan_init.restype = i32
+            lib.sdm_gather_plan_launch.argtypes = [vp, i64, i32, vp]
+            lib.sdm_gather_plan_launch.restype = i32
             lib.sdm_status_string.argtypes = [i32]
             lib.sdm_status_string.restype = ctypes.c_char_p
             lib.sdm_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint), i32]
@@ -238,6 +244,66 @@ def gather(bank, ops, *, chunk: int, valid: int | None = None, chunk_valid=None,
                               _stream_handle(stream, dev))
     _check("sdm_gather", rc)
     return outs, stash
+
+
+class GatherPlan:
+    """A checked no-stash gather launch replayed per slab (sdm_gather_plan_init / _launch).
+
+    ``ops = [(idx, w), ...]`` are the WHOLE index and weight tensors [rows, width]; every
+    ``launch(row0, valid)`` gathers their rows [row0, row0 + tokens) into ``outs`` (one [tokens,
+    hd] float32 tensor per operand, allocated when not given), with ``valid`` live tokens per
+    chunk. The plan keeps references to every tensor it was made with, so they stay alive while
+    it exists; they must not be resized or reallocated in place.
+    """
+
+    def __init__(self, bank, ops, *, tokens: int, chunk: int, row0_max: int | None = None, outs=None):
+        if bank.dtype not in _BANK_CODES or bank.dim() != 2:
+            raise TypeError("bank must be a [n_slots, head_dim] bfloat16 or float32 tensor")
+        dev = bank.device
+        _need(bank, "bank", dev)
+        if len(ops) not in (1, 2):
+            raise ValueError("gather takes one or two operands")
+        n_slots, hd = bank.shape
+        rows = ops[0][0].shape[0]
+        idx_dt, w_dt = ops[0][0].dtype, ops[0][1].dtype
+        if idx_dt not in _IDX_CODES or w_dt not in _BANK_CODES:
+            raise TypeError("indices must be int32/int64 and weights bfloat16/float32")
+        for o, (idx, w) in enumerate(ops):
+            _need(idx, f"idx[{o}]", dev)
+            _need(w, f"w[{o}]", dev)
+            if idx.dtype != idx_dt or w.dtype != w_dt:
+                raise TypeError("both operands must share the index dtype and the weight dtype")
+            if idx.dim() != 2 or idx.shape[0] != rows or tuple(w.shape) != tuple(idx.shape):
+                raise ValueError(f"operand {o}: idx and w must both be [rows, width] with the same rows")
+        if outs is None:
+            outs = [torch.empty((tokens, hd), dtype=torch.float32, device=dev) for _ in ops]
+        for o, out in enumerate(outs):
+            _need(out, f"out[{o}]", dev)
+            _f32(out, f"out[{o}]")
+            _shape(out, f"out[{o}]", (tokens, hd))
+        if row0_max is None:
+            row0_max = rows - tokens
+        vp = ctypes.c_void_p
+        n = len(ops)
+        idx_arr = (vp * 2)(*[vp(op[0].data_ptr()) for op in ops], *([vp(0)] * (2 - n)))
+        w_arr = (vp * 2)(*[vp(op[1].data_ptr()) for op in ops], *([vp(0)] * (2 - n)))
+        out_arr = (vp * 2)(*[vp(o.data_ptr()) for o in outs], *([vp(0)] * (2 - n)))
+        width_arr = (ctypes.c_int * 2)(*[op[0].shape[1] for op in ops], *([0] * (2 - n)))
+        self._record = ctypes.create_string_buffer(GATHER_PLAN_BYTES)
+        with torch.cuda.device(dev):
+            rc = library().sdm_gather_plan_init(self._record, bank.data_ptr(), n_slots, hd, _BANK_CODES[bank.dtype], n,
+                                                idx_arr, w_arr, out_arr, width_arr, _IDX_CODES[idx_dt],
+                                                _BANK_CODES[w_dt], rows, row0_max, tokens, chunk)
+        _check("sdm_gather_plan_init", rc)
+        self._keep = (bank, tuple(tuple(op) for op in ops))
+        self.outs, self.device, self.tokens, self.chunk, self.row0_max = outs, dev, tokens, chunk, row0_max
+
+    def launch(self, row0: int, valid: int | None = None, stream=None) -> list:
+        """The planned gather over index rows [row0, row0 + tokens); returns ``outs``."""
+        rc = library().sdm_gather_plan_launch(self._record, row0, self.chunk if valid is None else valid,
+                                              _stream_handle(stream, self.device))
+        _check("sdm_gather_plan_launch", rc)
+        return self.outs
 
 
 def device_status(clear: bool = True) -> int:

@@ -75,7 +75,7 @@ class GatherWorkload:
         return dataclasses.replace(self, **kw)
 
 
-# The five workloads: four decode shapes and one gather shape.
+# The five workloads: four decode shapes and one gather shape (plus the gather's backward shape).
 C0 = DecodeWorkload("decode_f32_s4_hd64_w8_t16", "f32", 4, 64, 1024, 8, 8, 1, 16, "i32", 1 / math.sqrt(8))
 C1 = DecodeWorkload("decode_bf16_s64_hd128_w32_gw_256steps", "bf16", 64, 128, 65536, 32, 32, 32, 256, "i64",
                     1 / math.sqrt(8), mode="step")
@@ -85,8 +85,13 @@ C3 = DecodeWorkload("decode_f32_s256_hd256_w256_t8", "f32", 256, 256, 8192, 256,
 C4 = GatherWorkload("gather_bf16_4M_hd128_65536tok_2x64_stash", "bf16", 4194304, 128, 65536, 64, (64, 64), "i64",
                     "bf16", 1 / 8)
 
+# The backward's one-operand shape of the same gather: bank-gradient rows (float32) at the write
+# slots weighted by the write weights, plus the stash of those rows.
+C4_BWD = GatherWorkload("gather_bwd_f32_4M_hd128_65536tok_1x64_stash", "f32", 4194304, 128, 65536, 64, (64,), "i64",
+                        "f32", 1 / 8)
+
 DECODE_WORKLOADS = {w.name: w for w in (C0, C1, C2, C3)}
-GATHER_WORKLOADS = {C4.name: C4}
+GATHER_WORKLOADS = {w.name: w for w in (C4, C4_BWD)}
 
 
 def _gen(device, seed: int) -> torch.Generator:

@@ -5,10 +5,14 @@
  *   sdm_decode_step  one write-then-read token for every stream
  *   sdm_decode_seq   T tokens for every stream in one persistent launch
  *   sdm_gather       per-token weighted sums of bank rows (one or two operands), optional stash
+ *                    (sdm_gather_kpos: with a compact snapshot instead; sdm_gather_plan_*: a
+ *                    checked launch, replayed per slab of an index tensor)
  *
  * Common rules
- *   - Every pointer argument except `stream` is a DEVICE pointer the caller owns; the library
- *     keeps no pointer after the call returns (apart from the work it enqueued) and frees nothing.
+ *   - Every pointer argument except `stream` (and the host records and arrays named as such) is a
+ *     DEVICE pointer the caller owns; the library keeps no pointer after the call returns (apart
+ *     from the work it enqueued, and from a gather plan record, which the caller owns and which
+ *     holds the pointers it was made with) and frees nothing.
  *   - Calls allocate no memory, synchronise nothing and only enqueue work on `stream` (NULL = the
  *     legacy default stream), so they may be captured in a CUDA graph.
  *   - Return value: 0 = launched (or nothing to do); < 0 = argument error (an SDM_E* code below,
@@ -59,6 +63,9 @@ typedef struct CUstream_st* sdm_stream_t;
 #define SDM_EALIGN (-9)     /* a pointer is not aligned to its element size */
 #define SDM_EOVERLAP (-10)  /* a gather output or the stash overlaps the bank */
 #define SDM_ENOPS (-11)     /* gather operand count is not 1 or 2 */
+#define SDM_EPLAN (-12)     /* not an initialised gather plan (wrong tag or record size) */
+#define SDM_EROW (-13)      /* row0 outside 0..row0_max, or row0_max + tokens beyond the index rows */
+#define SDM_EDEVICE (-14)   /* the current device is not the one the gather plan was made on */
 
 /* bits of the device status word */
 #define SDM_DEV_TIMEOUT 1u   /* reserved: a kernel gave up a bounded wait (no current kernel waits) */
@@ -155,6 +162,49 @@ int sdm_gather_kpos(const void* bank, int64_t n_slots, int hd, int bank_dtype, i
                     const void* const w[2], float* const out[2], const int width[2], int idx_dtype, int w_dtype,
                     void* compact, const int32_t* kpos, int64_t tokens, int chunk, int valid,
                     const int32_t* chunk_valid, sdm_stream_t stream);
+
+/*
+ * Gather launch plan (gather_cuda.py, token_gather_dc_plan / token_gather_dc_step): the checks
+ * and the launch geometry of a no-stash gather, done once; each step then only checks row0 and
+ * valid and relaunches the same kernel. Meant for a loop over the slabs of one index tensor:
+ * launch k reads index and weight rows [row0, row0 + tokens) and writes out[o][0 .. tokens).
+ *
+ * The plan is a caller-owned record (any memory the caller likes, usually a host stack or struct
+ * field); the library writes it in sdm_gather_plan_init and only reads it afterwards. It holds the
+ * device pointers it was given: they must stay valid (and the arrays unresized) while the plan is
+ * used. It is valid on the device that was current at init, in this process, until the library is
+ * unloaded. Copying the record copies the plan.
+ */
+#define SDM_GATHER_PLAN_BYTES 512
+typedef struct sdm_gather_plan {
+    uint64_t opaque[SDM_GATHER_PLAN_BYTES / 8];
+} sdm_gather_plan;
+
+/*
+ * sdm_gather_plan_init - check a no-stash sdm_gather once, at the largest row0 it will be used
+ * with, and record its launch in *plan. Nothing is launched.
+ *
+ *   plan       host pointer to the record to fill (written only when 0 is returned)
+ *   idx[o], w[o] [rows, width[o]]: the whole index / weight arrays of operand o (device)
+ *   out[o]     [tokens, hd] float32, written by every launch (device)
+ *   rows       index rows the arrays hold; row0_max >= 0 with row0_max + tokens <= rows
+ *   tokens, chunk  tokens per launch (>= 0, a multiple of chunk), chunk >= 1
+ * Other arguments as sdm_gather. Returns 0, an SDM_E* code, or a cudaError_t from the device
+ * queries (current device, multiprocessor count, occupancy).
+ */
+int sdm_gather_plan_init(sdm_gather_plan* plan, const void* bank, int64_t n_slots, int hd, int bank_dtype, int n_ops,
+                         const void* const idx[2], const void* const w[2], float* const out[2], const int width[2],
+                         int idx_dtype, int w_dtype, int64_t rows, int64_t row0_max, int64_t tokens, int chunk);
+
+/*
+ * sdm_gather_plan_launch - one step of a plan: the planned gather over index rows
+ * [row0, row0 + tokens) with `valid` live tokens per chunk (the tokens at t % chunk >= valid are
+ * padding, as in sdm_gather). Checks, in order: the record (SDM_EPLAN), 0 <= row0 <= row0_max
+ * (SDM_EROW), 0 <= valid <= chunk (SDM_ECHUNK), the current device (SDM_EDEVICE); then launches
+ * on `stream` exactly what sdm_gather would launch for the same rows. Returns 0, an SDM_E* code
+ * (nothing launched) or the cudaError_t of a failed launch.
+ */
+int sdm_gather_plan_launch(const sdm_gather_plan* plan, int64_t row0, int valid, sdm_stream_t stream);
 
 /* A static string naming a return code of the calls above. */
 const char* sdm_status_string(int status);

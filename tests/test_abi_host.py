@@ -155,3 +155,51 @@ def _gather_kpos(lib, **kw):
 ])
 def test_gather_kpos_argument_errors(lib, kw, code):
     assert _gather_kpos(lib, **kw) == CODES[code]
+
+
+def _plan_init(lib, record, **kw):
+    a = dict(bank=FAKE, n_slots=1000, hd=64, bank_dtype=0, n_ops=1, idx=(FAKE + (1 << 24), 0),
+             w=(FAKE + (3 << 24), 0), out=(FAKE + (5 << 24), 0), width=(8, 0), idx_dtype=1, w_dtype=0, rows=256,
+             row0_max=192, tokens=64, chunk=16)
+    a.update(kw)
+    vp = ctypes.c_void_p
+    return lib.sdm_gather_plan_init(record, a["bank"], a["n_slots"], a["hd"], a["bank_dtype"], a["n_ops"],
+                                    (vp * 2)(*a["idx"]), (vp * 2)(*a["w"]), (vp * 2)(*a["out"]),
+                                    (ctypes.c_int * 2)(*a["width"]), a["idx_dtype"], a["w_dtype"], a["rows"],
+                                    a["row0_max"], a["tokens"], a["chunk"])
+
+
+def test_plan_record_size_matches_header():
+    text = open(HEADER).read()
+    assert int(re.search(r"#define SDM_GATHER_PLAN_BYTES (\d+)", text).group(1)) == sdm.GATHER_PLAN_BYTES
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(row0_max=-1), "SDM_EROW"), (dict(row0_max=193), "SDM_EROW"), (dict(rows=63, row0_max=0), "SDM_EROW"),
+    (dict(chunk=5), "SDM_ECHUNK"), (dict(width=(0, 0)), "SDM_EWIDTH"), (dict(n_ops=3), "SDM_ENOPS"),
+    (dict(idx=(0, 0)), "SDM_ENULL"), (dict(out=(FAKE + 64, 0)), "SDM_EOVERLAP"), (dict(bank_dtype=4), "SDM_EDTYPE"),
+])
+def test_gather_plan_init_argument_errors(lib, kw, code):
+    record = ctypes.create_string_buffer(sdm.GATHER_PLAN_BYTES)
+    assert _plan_init(lib, record, **kw) == CODES[code]
+    assert record.raw == bytes(sdm.GATHER_PLAN_BYTES)  # nothing written on an error
+
+
+def test_gather_plan_init_null_record(lib):
+    assert _plan_init(lib, None) == CODES["SDM_ENULL"]
+
+
+def test_gather_plan_launch_refuses_a_foreign_record(lib):
+    zero = ctypes.create_string_buffer(sdm.GATHER_PLAN_BYTES)
+    assert lib.sdm_gather_plan_launch(zero, 0, 16, None) == CODES["SDM_EPLAN"]
+    junk = ctypes.create_string_buffer(bytes(range(256)) * 2)
+    assert lib.sdm_gather_plan_launch(junk, 0, 16, None) == CODES["SDM_EPLAN"]
+    assert lib.sdm_gather_plan_launch(None, 0, 16, None) == CODES["SDM_ENULL"]
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-device answer")
+def test_gather_plan_init_without_a_device_reports_the_cuda_error(lib):
+    record = ctypes.create_string_buffer(sdm.GATHER_PLAN_BYTES)
+    rc = _plan_init(lib, record)
+    assert rc > 0 and sdm.status_string(rc)
+    assert record.raw == bytes(sdm.GATHER_PLAN_BYTES)

@@ -125,21 +125,23 @@ def test_gather_out_of_range_index_is_skipped_and_flagged():
     assert bits_equal(to_np(stash), rs)
 
 
-def test_gather_full_size():
-    """The full gather workload in the benchmark's launch configuration: sampled tokens against the
-    oracle bit for bit, every stash row against torch's own row indexing, every padding token zero,
-    and every output within the float32 summation bound of a float64 evaluation."""
-    wl = workloads.C4
+@pytest.mark.parametrize("wl", [workloads.C4, workloads.C4_BWD], ids=lambda w: w.name)
+def test_gather_full_size(wl):
+    """A full gather workload in the benchmark's launch configuration (the two-operand forward
+    shape and the one-operand backward shape): sampled tokens against the oracle bit for bit,
+    every stash row against torch's own row indexing, every padding token zero, and every output
+    within the float32 summation bound of a float64 evaluation."""
     g = workloads.make_gather_inputs(wl, device=DEV)
     outs, stash = sdm.gather(g["bank"], g["ops"], chunk=wl.chunk, chunk_valid=g["chunk_valid"])
     torch.cuda.synchronize()
     assert sdm.device_status() == 0
     live = (torch.arange(wl.tokens, device=DEV) % wl.chunk) < g["chunk_valid"].repeat_interleave(wl.chunk)
-    (i0, w0), (i1, w1) = g["ops"]
+    i0 = g["ops"][0][0]
+    bits = torch.int16 if wl.bank_dtype == "bf16" else torch.int32
     # stash: raw rows, bit-exact (torch's indexing as the independent reference); padding rows zero
     ref_stash = g["bank"][i0[live]]
-    assert torch.equal(stash[live].view(torch.int16), ref_stash.view(torch.int16))
-    assert not stash[~live].view(torch.int16).any()
+    assert torch.equal(stash[live].view(bits), ref_stash.view(bits))
+    assert not stash[~live].view(bits).any()
     for o, (idx, w) in enumerate(g["ops"]):
         out = outs[o]
         assert not out[~live].any()
