@@ -22,9 +22,11 @@
 //      retrieve as one chain of paired fmas over ascending w, then delta, then the decay-and-write
 //      (paired multiply and fma, one paired round to the bank dtype, one store per row);
 //   3. a barrier, then the R read rows by 16-byte cp.async, and each thread reduces its columns
-//      over ascending r;
+//      over ascending r (for bf16 banks with the mixed-precision fma, whose bf16 operands need no
+//      widening); meanwhile the next token's write rows are prefetched into L2, so that its
+//      copies in step 1 are served from L2 while their DRAM reads overlap this step;
 //   4. the prefetched metadata of the next token is turned into row byte offsets and broadcast
-//      weight pairs in shared memory.
+//      weight pairs in shared memory (16-byte aligned arrays, read two rows' worth per load).
 // The rows travel as 16-byte cp.async copies (the load/store path, generic proxy) rather than one
 // bulk copy per row: with 256-byte rows the bulk-copy engine sustained about 3 TB/s of row reads
 // per GPU, the 16-byte copies spread over all threads sustain the rest of HBM. Being generic-proxy
@@ -73,6 +75,18 @@ __device__ __forceinline__ uint64_t fmul2(uint64_t a, uint64_t b) {
     return d;
 }
 
+// lo += q * x.lo, hi += q * x.hi for a bf16 pair x, with q the bf16 held in the high half of the
+// float32 bit pattern qbits (exact when the float32 is bf16-representable); one rounding each
+__device__ __forceinline__ void fma_bf16_pair(float& lo, float& hi, uint32_t qbits, uint32_t x) {
+    asm("{\n\t.reg .b16 xl, xh, ql, qh;\n\t"
+        "mov.b32 {xl, xh}, %2;\n\t"
+        "mov.b32 {ql, qh}, %3;\n\t"
+        "fma.rn.f32.bf16 %0, qh, xl, %0;\n\t"
+        "fma.rn.f32.bf16 %1, qh, xh, %1;\n\t}"
+        : "+f"(lo), "+f"(hi)
+        : "r"(x), "r"(qbits));
+}
+
 // two adjacent bank elements as one word, widened to / narrowed from a float32 pair
 template <typename E>
 struct Pair;
@@ -108,12 +122,12 @@ struct VecLayout {
         raw_qv = align_up(raw_q + (size_t)R * is, 16);
         raw_beta = align_up(raw_qv + (size_t)R * 4, 16);
         koff = align_up(raw_beta + 4, 16);
-        qoff = koff + (size_t)W * 8;
-        aw2 = qoff + (size_t)R * 8;
-        kv2 = aw2 + (size_t)W * 8;
-        dw2 = kv2 + (size_t)W * 8;
-        qv2 = dw2 + (size_t)W * 8;
-        beta = qv2 + (size_t)R * 8;
+        qoff = align_up(koff + (size_t)W * 8, 16);
+        aw2 = align_up(qoff + (size_t)R * 8, 16);
+        kv2 = align_up(aw2 + (size_t)W * 8, 16);
+        dw2 = align_up(kv2 + (size_t)W * 8, 16);
+        qv2 = align_up(dw2 + (size_t)W * 8, 16);
+        beta = align_up(qv2 + (size_t)R * 8, 16);
         dnext = beta + 4;
         total = dnext + 4;
     }
@@ -291,40 +305,91 @@ __global__ void __launch_bounds__(kMaxThreads, 2) decode_vec_kernel(const Decode
             for (; w + 4 <= W; w += 4) {
                 const PT x0 = rp[(w + 0) * pstride], x1 = rp[(w + 1) * pstride];
                 const PT x2 = rp[(w + 2) * pstride], x3 = rp[(w + 3) * pstride];
-                acc = ffma2(aw2[w + 0], P::widen(x0), acc);
-                acc = ffma2(aw2[w + 1], P::widen(x1), acc);
-                acc = ffma2(aw2[w + 2], P::widen(x2), acc);
-                acc = ffma2(aw2[w + 3], P::widen(x3), acc);
+                const ulonglong2 a01 = *reinterpret_cast<const ulonglong2*>(aw2 + w);
+                const ulonglong2 a23 = *reinterpret_cast<const ulonglong2*>(aw2 + w + 2);
+                acc = ffma2(a01.x, P::widen(x0), acc);
+                acc = ffma2(a01.y, P::widen(x1), acc);
+                acc = ffma2(a23.x, P::widen(x2), acc);
+                acc = ffma2(a23.y, P::widen(x3), acc);
             }
             for (; w < W; ++w) acc = ffma2(aw2[w], P::widen(rp[w * pstride]), acc);
             const float dl = __fmul_rn(beta, __fsub_rn(f2lo(vr), f2lo(acc)));
             const float dh = __fmul_rn(beta, __fsub_rn(f2hi(vr), f2hi(acc)));
             const uint64_t delta = f2(dl, dh);
-#pragma unroll 4
-            for (w = 0; w < W; ++w) {
+            unsigned char* bj = bank + jb;
+            w = 0;
+#pragma unroll 2
+            for (; w + 2 <= W; w += 2) {
+                const uint64_t x0 = P::widen(rp[w * pstride]), x1 = P::widen(rp[(w + 1) * pstride]);
+                const ulonglong2 k2 = *reinterpret_cast<const ulonglong2*>(kv2 + w);
+                const longlong2 o2 = *reinterpret_cast<const longlong2*>(koff + w);
+                uint64_t d0 = dsh, d1 = dsh;
+                if (G != 1) {
+                    const ulonglong2 dd = *reinterpret_cast<const ulonglong2*>(dw2 + w);
+                    d0 = dd.x;
+                    d1 = dd.y;
+                }
+                const uint64_t y0 = ffma2(k2.x, delta, fmul2(x0, d0));
+                const uint64_t y1 = ffma2(k2.y, delta, fmul2(x1, d1));
+                *reinterpret_cast<PT*>(bj + o2.x) = P::narrow(y0);
+                *reinterpret_cast<PT*>(bj + o2.y) = P::narrow(y1);
+            }
+            for (; w < W; ++w) {
                 const uint64_t x = P::widen(rp[w * pstride]);
                 const uint64_t y = ffma2(kv2[w], delta, fmul2(x, G == 1 ? dsh : dw2[w]));
-                *reinterpret_cast<PT*>(bank + koff[w] + jb) = P::narrow(y);
+                *reinterpret_cast<PT*>(bj + koff[w]) = P::narrow(y);
             }
         }
+        if (more) cp_async_wait_all();  // the next token's slots have landed
         __syncthreads();
 
-        // 3. the read rows, after the write
+        // 3. the read rows, after the write; the next token's write rows are warmed in L2 meanwhile
         ldgsts_rows<E>(rows, bank, qoff, R, sw, row_bytes);
+        if (more) {
+            const I* rk = reinterpret_cast<const I*>(smem + L.raw_k);
+            const int lines = (int)((row_bytes + 127) >> 7);
+            const int64_t rowb = (int64_t)hd * ES, colb = (int64_t)c0 * ES;
+            for (int i = tid; i < W * lines; i += blockDim.x) {
+                const int r = i / lines, l = i - r * lines;
+                const unsigned char* p = bank + (int64_t)rk[r] * rowb + colb + (int64_t)l * 128;
+                asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+            }
+        }
         cp_async_wait_all();
         __syncthreads();
         if (active) {
             uint64_t acc = 0;
             int r = 0;
-            for (; r + 4 <= R; r += 4) {
-                const PT x0 = rp[(r + 0) * pstride], x1 = rp[(r + 1) * pstride];
-                const PT x2 = rp[(r + 2) * pstride], x3 = rp[(r + 3) * pstride];
-                acc = ffma2(qv2[r + 0], P::widen(x0), acc);
-                acc = ffma2(qv2[r + 1], P::widen(x1), acc);
-                acc = ffma2(qv2[r + 2], P::widen(x2), acc);
-                acc = ffma2(qv2[r + 3], P::widen(x3), acc);
+            if constexpr (sizeof(E) == 2) {
+                // bf16 rows: the rounded read weight and the row element are both bf16, so the
+                // mixed-precision fma (bf16 operands, float32 accumulator, one rounding) gives the
+                // same float32 as widening both and using fmaf
+                float lo = 0.0f, hi = 0.0f;
+                for (; r + 4 <= R; r += 4) {
+                    const uint32_t x0 = rp[(r + 0) * pstride], x1 = rp[(r + 1) * pstride];
+                    const uint32_t x2 = rp[(r + 2) * pstride], x3 = rp[(r + 3) * pstride];
+                    const uint4 q = *reinterpret_cast<const uint4*>(qv2 + r);  // low words: float32 bits
+                    const uint4 q2 = *reinterpret_cast<const uint4*>(qv2 + r + 2);
+                    fma_bf16_pair(lo, hi, q.x, x0);
+                    fma_bf16_pair(lo, hi, q.z, x1);
+                    fma_bf16_pair(lo, hi, q2.x, x2);
+                    fma_bf16_pair(lo, hi, q2.z, x3);
+                }
+                for (; r < R; ++r) fma_bf16_pair(lo, hi, (uint32_t)qv2[r], rp[r * pstride]);
+                acc = f2(lo, hi);
+            } else {
+                for (; r + 4 <= R; r += 4) {
+                    const PT x0 = rp[(r + 0) * pstride], x1 = rp[(r + 1) * pstride];
+                    const PT x2 = rp[(r + 2) * pstride], x3 = rp[(r + 3) * pstride];
+                    const ulonglong2 q01 = *reinterpret_cast<const ulonglong2*>(qv2 + r);
+                    const ulonglong2 q23 = *reinterpret_cast<const ulonglong2*>(qv2 + r + 2);
+                    acc = ffma2(q01.x, P::widen(x0), acc);
+                    acc = ffma2(q01.y, P::widen(x1), acc);
+                    acc = ffma2(q23.x, P::widen(x2), acc);
+                    acc = ffma2(q23.y, P::widen(x3), acc);
+                }
+                for (; r < R; ++r) acc = ffma2(qv2[r], P::widen(rp[r * pstride]), acc);
             }
-            for (; r < R; ++r) acc = ffma2(qv2[r], P::widen(rp[r * pstride]), acc);
             *reinterpret_cast<PT*>(out + ts * hd + c0 + j) = P::narrow(acc);
         }
 
