@@ -126,7 +126,7 @@ struct VecLayout {
         aw2 = align_up(qoff + (size_t)R * 8, 16);
         kv2 = align_up(aw2 + (size_t)W * 8, 16);
         dw2 = align_up(kv2 + (size_t)W * 8, 16);
-        qv2 = align_up(dw2 + (size_t)W * 8, 16);
+        qv2 = align_up(dw2 + (size_t)(G == 1 ? 1 : W) * 8, 16);  // one shared gate when G == 1
         beta = align_up(qv2 + (size_t)R * 8, 16);
         dnext = beta + 4;
         total = dnext + 4;
@@ -197,7 +197,7 @@ __device__ __forceinline__ void derive_meta(const DecodeArgs& a, int c0, const V
         const float aa = __fmul_rn(k, d);
         kv2[i] = f2(k, k);
         aw2[i] = f2(aa, aa);
-        dw2[i] = f2(d, d);
+        if (G != 1 || i == 0) dw2[i] = f2(d, d);
     }
     for (int i = tid; i < R; i += nt) {
         qoff[i] = (int64_t)rq[i] * rowb + colb;
@@ -407,17 +407,20 @@ __global__ void __launch_bounds__(kMaxThreads, 2) decode_vec_kernel(const Decode
 // 1 KiB), the rows stream through a ring of NS chunk buffers of CH rows each instead of being
 // staged all at once: the write rows pass twice (retrieve, then decay-and-write; the second pass
 // is served mostly by L2) and the read rows once. Chunks are consumed in ascending row order, so
-// every sum keeps the order and the bits of the staged path.
+// every sum keeps the order and the bits of the staged path. CH is chosen at launch: the largest
+// chunk (kStreamRowsMin..kStreamRowsMax rows) whose ring still lets every block of the grid be
+// resident at once; larger chunks put more rows in flight and take fewer barriers per pass.
 
-constexpr int kStreamRows = 16;   // rows per chunk
-constexpr int kStreamStages = 4;  // chunk buffers in the ring
+constexpr int kStreamRowsMin = 16;  // rows per chunk, at least
+constexpr int kStreamRowsMax = 32;  // and at most
+constexpr int kStreamStages = 4;    // chunk buffers in the ring
 
 struct StreamLayout {
     VecLayout meta;  // the metadata of the staged layout, with no row area
     size_t ring, total;
-    __host__ __device__ StreamLayout(int W, int R, int G, int sw, int es, int is) : meta(W, R, G, 0, es, is) {
+    __host__ __device__ StreamLayout(int W, int R, int G, int sw, int es, int is, int ch) : meta(W, R, G, 0, es, is) {
         ring = align_up(meta.total, 128);
-        total = ring + (size_t)kStreamStages * kStreamRows * sw * es;
+        total = ring + (size_t)kStreamStages * ch * sw * es;
     }
 };
 
@@ -433,11 +436,12 @@ __global__ void __launch_bounds__(kMaxThreads, 1) decode_stream_kernel(const Dec
     using P = Pair<E>;
     using PT = typename P::T;
     constexpr int ES = sizeof(E);
-    constexpr int NS = kStreamStages, CH = kStreamRows;
+    constexpr int NS = kStreamStages;
+    const int CH = a.stream_rows;
     extern __shared__ __align__(128) unsigned char smem[];
 
     const int W = a.W, R = a.R, G = a.G, hd = a.hd, sw = a.slice_cols;
-    const StreamLayout SL(W, R, G, sw, ES, (int)sizeof(I));
+    const StreamLayout SL(W, R, G, sw, ES, (int)sizeof(I), CH);
     const VecLayout& L = SL.meta;
     unsigned char* ring = smem + SL.ring;
     const size_t stage_bytes = (size_t)CH * sw * ES;
@@ -712,10 +716,23 @@ int launch_decode(const DecodeArgs& a0, int bank_dtype, int idx_dtype, cudaStrea
     a.n_slices = (a.hd + sw - 1) / sw;
     const int64_t blocks = a.n_streams * a.n_slices;
     if (blocks > INT_MAX) return SDM_ECOUNT;
+    a.stream_rows = kStreamRowsMin;
+    if (streamed) {  // the largest chunk that keeps the whole grid resident in one wave
+        const int64_t per_sm = (blocks + sm_count() - 1) / sm_count();
+        const size_t meta = StreamLayout(a.W, a.R, a.G, sw, es, is, 0).total;
+        const size_t block_budget = smem_per_sm() / (size_t)per_sm;
+        const size_t reserve = smem_reserved_per_block();
+        const size_t stage_row = (size_t)kStreamStages * sw * es;
+        if (block_budget > meta + reserve) {
+            const int64_t fit = (int64_t)((block_budget - meta - reserve) / stage_row);
+            const int most = std::min(kStreamRowsMax, std::max(maxwr, kStreamRowsMin));
+            a.stream_rows = (int)std::max<int64_t>(kStreamRowsMin, std::min<int64_t>(fit, most));
+        }
+    }
     const int threads = ((sw + cpt - 1) / cpt + 31) / 32 * 32;
     const int path = !vec ? kSimt : streamed ? kStream : kStaged;
     const size_t smem = path == kStaged   ? VecLayout(a.W, a.R, a.G, sw, es, is).total
-                        : path == kStream ? StreamLayout(a.W, a.R, a.G, sw, es, is).total
+                        : path == kStream ? StreamLayout(a.W, a.R, a.G, sw, es, is, a.stream_rows).total
                                           : SimtLayout(a.W, a.R, sw, es).total;
 
     const dim3 grid((unsigned)blocks), block((unsigned)threads);

@@ -30,6 +30,40 @@ int sm_count() {
     return n;
 }
 
+namespace {
+
+// A device attribute of the current device, cached per device; `fallback` when it cannot be read.
+int device_attribute(std::atomic<int>* cache, cudaDeviceAttr attr, int fallback) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return fallback;
+    }
+    if (dev >= 0 && dev < 64) {
+        const int c = cache[dev].load(std::memory_order_relaxed);
+        if (c > 0) return c;
+    }
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, attr, dev) != cudaSuccess || n <= 0) {
+        (void)cudaGetLastError();
+        return fallback;
+    }
+    if (dev >= 0 && dev < 64) cache[dev].store(n, std::memory_order_relaxed);
+    return n;
+}
+
+}  // namespace
+
+size_t smem_per_sm() {
+    static std::atomic<int> cache[64];
+    return (size_t)device_attribute(cache, cudaDevAttrMaxSharedMemoryPerMultiprocessor, 228 * 1024);
+}
+
+size_t smem_reserved_per_block() {
+    static std::atomic<int> cache[64];
+    return (size_t)device_attribute(cache, cudaDevAttrReservedSharedMemoryPerBlock, 1024);
+}
+
 }  // namespace sdm
 
 namespace {

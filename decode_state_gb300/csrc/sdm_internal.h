@@ -19,8 +19,9 @@ struct DecodeArgs {
     void* out;
     int64_t n_streams;
     int hd, W, R, G, T;
-    int slice_cols;  // columns one block owns (the last slice may be narrower)
-    int n_slices;    // ceil(hd / slice_cols)
+    int slice_cols;   // columns one block owns (the last slice may be narrower)
+    int n_slices;     // ceil(hd / slice_cols)
+    int stream_rows;  // rows per ring chunk of the streaming path
 };
 
 struct GatherArgs {
@@ -62,6 +63,10 @@ int gather_status(unsigned int* word, bool clear);
 
 // Multiprocessor count of the current device (cached per device).
 int sm_count();
+// Shared memory of one multiprocessor, and the part the system reserves per block, in bytes
+// (current device, cached per device).
+size_t smem_per_sm();
+size_t smem_reserved_per_block();
 
 // Launch the kernel at address `kernel` (arguments as an array of pointers to them) with
 // programmatic stream serialization (see grid_dependency_wait). Returns a cudaError_t. Raises the
