@@ -16,8 +16,10 @@
 //
 // Vector path (rows a multiple of 16 bytes), per token:
 //   1. every thread issues 16-byte cp.async copies of the W write row slices into shared memory
-//      (all in flight at once), then cp.async copies of the NEXT token's slots and weights, and
-//      thread 0 computes the next token's shared gate;
+//      (all in flight at once), L2 prefetches of this token's R read rows (only a hint: the
+//      copies in step 3 still read the rows as the write left them, from L2), then cp.async
+//      copies of the NEXT token's slots and weights, and thread 0 computes the next token's
+//      shared gate;
 //   2. each thread owns two adjacent columns, held as a packed float32 pair, and runs the
 //      retrieve as one chain of paired fmas over ascending w, then delta, then the decay-and-write
 //      (paired multiply and fma, one paired round to the bank dtype, one store per row);
@@ -279,6 +281,13 @@ __global__ void __launch_bounds__(kMaxThreads, 2) decode_vec_kernel(const Decode
 
         // 1. the write rows; the next token's metadata meanwhile
         ldgsts_rows<E>(rows, bank, koff, W, sw, row_bytes);
+        {  // this token's read rows into L2 meanwhile: step 3 then copies them from L2
+            const int lines = (int)((row_bytes + 127) >> 7);
+            for (int i = tid; i < R * lines; i += blockDim.x) {
+                const int r = i / lines, l = i - r * lines;
+                asm volatile("prefetch.global.L2 [%0];" ::"l"(bank + qoff[r] + (int64_t)l * 128));
+            }
+        }
         uint64_t vr = 0;
         if (active) {
             const float2 vv = __ldg(reinterpret_cast<const float2*>(a.v + ts * hd + c0 + j));
