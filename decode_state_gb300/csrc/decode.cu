@@ -22,7 +22,11 @@
 //      shared gate;
 //   2. each thread owns two adjacent columns, held as a packed float32 pair, and runs the
 //      retrieve as one chain of paired fmas over ascending w, then delta, then the decay-and-write
-//      (paired multiply and fma, one paired round to the bank dtype, one store per row);
+//      (paired multiply and fma, one paired round to the bank dtype). With many blocks per SM the
+//      owners publish their delta pairs and the write goes by 16-byte pieces instead (thread =
+//      row group and piece, one 16-byte load and store per row it takes), which needs a quarter
+//      of the per-row loads, stores and address work; otherwise each thread writes its own pair
+//      of every row;
 //   3. a barrier, then the R read rows by 16-byte cp.async, and each thread reduces its columns
 //      over ascending r (for bf16 banks with the mixed-precision fma, whose bf16 operands need no
 //      widening); meanwhile the next token's write rows are prefetched into L2, so that its
@@ -113,7 +117,7 @@ struct Pair<float> {
 // ---------------------------------------------------------------- vector-path layout
 
 struct VecLayout {
-    size_t rows, raw_k, raw_kv, raw_g, raw_q, raw_qv, raw_beta, koff, qoff, aw2, kv2, dw2, qv2, beta, dnext, total;
+    size_t rows, raw_k, raw_kv, raw_g, raw_q, raw_qv, raw_beta, koff, qoff, aw2, kv2, dw2, qv2, beta, dnext, dlt, total;
     __host__ __device__ VecLayout(int W, int R, int G, int sw, int es, int is) {
         const int maxwr = W > R ? W : R;
         rows = 0;
@@ -131,7 +135,8 @@ struct VecLayout {
         qv2 = align_up(dw2 + (size_t)(G == 1 ? 1 : W) * 8, 16);  // one shared gate when G == 1
         beta = align_up(qv2 + (size_t)R * 8, 16);
         dnext = beta + 4;
-        total = dnext + 4;
+        dlt = align_up(dnext + 4, 16);  // the delta pair of every column pair of the slice
+        total = dlt + (size_t)(sw / 2) * 8;
     }
 };
 
@@ -264,6 +269,9 @@ __global__ void __launch_bounds__(kMaxThreads, 2) decode_vec_kernel(const Decode
     E* out = static_cast<E*>(a.out);
     const PT* rp = reinterpret_cast<const PT*>(rows) + tid;
     const int64_t jb = (int64_t)j * ES;
+    const int nt = blockDim.x;
+    const int cpr = (int)(row_bytes >> 4);  // 16-byte pieces per row slice
+    const bool by_piece = a.piece_write && nt % cpr == 0 && nt / cpr <= W;
 
     grid_dependency_wait();
     if (early_trigger) grid_launch_dependents();
@@ -325,6 +333,9 @@ __global__ void __launch_bounds__(kMaxThreads, 2) decode_vec_kernel(const Decode
             const float dl = __fmul_rn(beta, __fsub_rn(f2lo(vr), f2lo(acc)));
             const float dh = __fmul_rn(beta, __fsub_rn(f2hi(vr), f2hi(acc)));
             const uint64_t delta = f2(dl, dh);
+            if (by_piece) {
+                reinterpret_cast<uint64_t*>(smem + L.dlt)[tid] = delta;
+            } else {
             unsigned char* bj = bank + jb;
             w = 0;
 #pragma unroll 2
@@ -347,6 +358,37 @@ __global__ void __launch_bounds__(kMaxThreads, 2) decode_vec_kernel(const Decode
                 const uint64_t x = P::widen(rp[w * pstride]);
                 const uint64_t y = ffma2(kv2[w], delta, fmul2(x, G == 1 ? dsh : dw2[w]));
                 *reinterpret_cast<PT*>(bj + koff[w]) = P::narrow(y);
+            }
+            }
+        }
+        if (by_piece) {
+            // the decay-and-write by 16-byte pieces: thread = (row group, piece); every thread
+            // takes one piece of every ngroups-th row, with the delta pairs its owners published
+            __syncthreads();
+            constexpr int PP = 16 / (2 * ES);  // column pairs per piece
+            const int k = tid % cpr, ngroups = nt / cpr;
+            uint64_t dp[PP];
+#pragma unroll
+            for (int p = 0; p < PP; ++p) dp[p] = reinterpret_cast<const uint64_t*>(smem + L.dlt)[k * PP + p];
+            const unsigned char* src = reinterpret_cast<const unsigned char*>(rows) + k * 16;
+            unsigned char* dst = bank + k * 16;
+            const size_t rstride = (size_t)sw * ES;
+#pragma unroll 2
+            for (int w = tid / cpr; w < W; w += ngroups) {
+                const uint4 x = *reinterpret_cast<const uint4*>(src + w * rstride);
+                const uint64_t d = G == 1 ? dsh : dw2[w], kv = kv2[w];
+                uint4 y;
+                if constexpr (ES == 2) {
+                    y.x = P::narrow(ffma2(kv, dp[0], fmul2(P::widen(x.x), d)));
+                    y.y = P::narrow(ffma2(kv, dp[1], fmul2(P::widen(x.y), d)));
+                    y.z = P::narrow(ffma2(kv, dp[2], fmul2(P::widen(x.z), d)));
+                    y.w = P::narrow(ffma2(kv, dp[3], fmul2(P::widen(x.w), d)));
+                } else {
+                    const uint64_t y0 = ffma2(kv, dp[0], fmul2(((uint64_t)x.y << 32) | x.x, d));
+                    const uint64_t y1 = ffma2(kv, dp[PP - 1], fmul2(((uint64_t)x.w << 32) | x.z, d));
+                    y = make_uint4((uint32_t)y0, (uint32_t)(y0 >> 32), (uint32_t)y1, (uint32_t)(y1 >> 32));
+                }
+                *reinterpret_cast<uint4*>(dst + koff[w]) = y;
             }
         }
         if (more) cp_async_wait_all();  // the next token's slots have landed
@@ -725,6 +767,9 @@ int launch_decode(const DecodeArgs& a0, int bank_dtype, int idx_dtype, cudaStrea
     a.n_slices = (a.hd + sw - 1) / sw;
     const int64_t blocks = a.n_streams * a.n_slices;
     if (blocks > INT_MAX) return SDM_ECOUNT;
+    // decay-and-write by pieces costs one more barrier per token: worth it when the SMs are full
+    // (bandwidth-bound), not when a few blocks per SM wait on latency
+    a.piece_write = blocks >= 4LL * sm_count() ? 1 : 0;
     a.stream_rows = kStreamRowsMin;
     if (streamed) {  // the largest chunk that keeps the whole grid resident in one wave
         const int64_t per_sm = (blocks + sm_count() - 1) / sm_count();

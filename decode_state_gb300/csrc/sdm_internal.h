@@ -22,6 +22,7 @@ struct DecodeArgs {
     int slice_cols;   // columns one block owns (the last slice may be narrower)
     int n_slices;     // ceil(hd / slice_cols)
     int stream_rows;  // rows per ring chunk of the streaming path
+    int piece_write;  // staged path: decay-and-write by 16-byte pieces (many blocks per SM)
 };
 
 struct GatherArgs {
