@@ -193,6 +193,21 @@ def oracle_stream_tokens(x: dict, streams, P: int):
     return done, secs
 
 
+def _oracle_worker(job):
+    """One process of the all-cores CPU baseline: the oracle `reps` times over `streams` streams of
+    the decode workload, drawn on the host from the job's own seed. Returns (stream-tokens, start,
+    end), wall-clock seconds around the oracle calls."""
+    fields, seed, streams, reps = job
+    wl = workloads.DecodeWorkload(**fields).scaled(n_streams=streams)
+    x = workloads.make_decode_inputs(wl, device="cpu", seed=seed)
+    oracle_stream_tokens(x, [0], wl.slots_per_stream)  # loads the oracle library
+    t0 = time.time()
+    done = 0
+    for _ in range(reps):
+        done += oracle_stream_tokens(x, range(streams), wl.slots_per_stream)[0]
+    return done, t0, time.time()
+
+
 def oracle_gather_tokens(bank_h, g: dict, tokens, chunk: int):
     """Oracle run over a list of gather tokens (host copies); returns (tokens, seconds)."""
     import oracle
@@ -383,6 +398,29 @@ class Case:
             sample = (f"{done} of {self.wl.tokens} tokens of the benchmark's own inputs "
                       f"(padding included, {secs:.1f} s single-threaded)")
         return {"value": done / secs, "unit": self.unit, "cores": 1, "kind": "oracle", "sample": sample}
+
+    def cpu_baseline_all_cores(self, budget_s: float, single: dict):
+        """The oracle on every host core at once: one process per core (spawn: CUDA is already
+        initialised here), each over its own streams of the same workload recipe. The value is all
+        processes' stream-tokens over the wall-clock span from the first start to the last end."""
+        if not self.kind.startswith("decode"):
+            return None
+        import dataclasses
+        import multiprocessing as mp
+
+        cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
+        streams = min(8, self.wl.n_streams)
+        per_rep_s = streams * self.wl.T / max(single["value"], 1e-9)
+        reps = max(1, int(budget_s / per_rep_s))
+        jobs = [(dataclasses.asdict(self.wl), 1000 + i, streams, reps) for i in range(cores)]
+        with mp.get_context("spawn").Pool(cores) as pool:
+            res = pool.map(_oracle_worker, jobs)
+        done = sum(r[0] for r in res)
+        span = max(r[2] for r in res) - min(r[1] for r in res)
+        sample = (f"{cores} processes at once, each {reps} passes over {streams} streams x {self.wl.T} tokens drawn "
+                  f"with the workload's recipe (seeds 1000..{999 + cores}); {done} stream-tokens in {span:.1f} s "
+                  f"of wall clock")
+        return {"value": done / span, "unit": self.unit, "cores": cores, "kind": "oracle", "sample": sample}
 
 
 # ---------------------------------------------------------------- our arm
@@ -576,6 +614,8 @@ def main():
         res, case = run_ours(args, r)
         if r.is_root:
             res["cpu_baseline"] = case.cpu_baseline(args.cpu_seconds)
+        if r.is_root and r.world == 1 and not args.no_extras:
+            res["cpu_baseline_all_cores"] = case.cpu_baseline_all_cores(args.cpu_seconds / 2, res["cpu_baseline"])
         del case
         torch.cuda.empty_cache()
         if r.is_root and r.world == 1 and not args.no_extras:
