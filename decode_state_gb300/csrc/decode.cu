@@ -240,7 +240,9 @@ __device__ __forceinline__ void ldgsts_rows(E* rows, const unsigned char* bank, 
     cp_async_commit();
 }
 
-template <typename E, typename I>
+// PIECE = false compiles the per-pair write-back only (the instance for grids of few blocks per SM,
+// where it runs faster without the piece path beside it).
+template <typename E, typename I, bool PIECE>
 __global__ void __launch_bounds__(kMaxThreads, 2) decode_vec_kernel(const DecodeArgs a, int early_trigger) {
     using P = Pair<E>;
     using PT = typename P::T;
@@ -271,7 +273,7 @@ __global__ void __launch_bounds__(kMaxThreads, 2) decode_vec_kernel(const Decode
     const int64_t jb = (int64_t)j * ES;
     const int nt = blockDim.x;
     const int cpr = (int)(row_bytes >> 4);  // 16-byte pieces per row slice
-    const bool by_piece = a.piece_write && nt % cpr == 0 && nt / cpr <= W;
+    const bool by_piece = PIECE && a.piece_write && nt % cpr == 0 && nt / cpr <= W;
 
     grid_dependency_wait();
     if (early_trigger) grid_launch_dependents();
@@ -722,7 +724,7 @@ enum Path { kSimt = 0, kStaged = 1, kStream = 2 };
 
 template <typename E, typename I>
 int launch_typed(int path, const DecodeArgs& a, dim3 grid, dim3 block, size_t smem, cudaStream_t stream) {
-    const auto kernel = path == kStaged ? decode_vec_kernel<E, I>
+    const auto kernel = path == kStaged   ? (a.piece_write ? decode_vec_kernel<E, I, true> : decode_vec_kernel<E, I, false>)
                         : path == kStream ? decode_stream_kernel<E, I>
                                           : decode_simt_kernel<E, I>;
     const int early = fits_one_wave(kernel, grid.x, (int)block.x, smem) ? 1 : 0;
