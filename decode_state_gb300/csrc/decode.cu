@@ -753,7 +753,8 @@ int launch_decode(const DecodeArgs& a0, int bank_dtype, int idx_dtype, cudaStrea
     // Column slice: the whole row when it fits; narrower to bound shared memory and to give the
     // grid at least two blocks per SM when there are few streams. When staging every row would
     // force slices narrower than 256 bytes (wide rows with many writes or reads), the rows stream
-    // through a chunk ring instead, with slices of up to 512 bytes.
+    // through a chunk ring instead, with slices of up to 512 bytes (or whole rows of up to 1 KiB,
+    // chosen below).
     const int full = vec ? std::min(a.hd, kMaxThreads * cpt) / q * q : std::min(a.hd, kMaxThreads * cpt);
     int sw = full;
     while ((size_t)maxwr * sw * es > kRowsBudget && sw > q) sw = shrink_cols(sw, q);
@@ -773,25 +774,44 @@ int launch_decode(const DecodeArgs& a0, int bank_dtype, int idx_dtype, cudaStrea
     // (bandwidth-bound), not when a few blocks per SM wait on latency
     a.piece_write = blocks >= 4LL * sm_count() ? 1 : 0;
     a.stream_rows = kStreamRowsMin;
-    if (streamed) {  // the largest chunk that keeps the whole grid resident in one wave
-        const int64_t per_sm = (blocks + sm_count() - 1) / sm_count();
-        const size_t meta = StreamLayout(a.W, a.R, a.G, sw, es, is, 0).total;
-        const size_t block_budget = smem_per_sm() / (size_t)per_sm;
-        const size_t reserve = smem_reserved_per_block();
-        const size_t stage_row = (size_t)kStreamStages * sw * es;
-        if (block_budget > meta + reserve) {
+    if (streamed) {
+        // the largest chunk that keeps the whole grid resident in one wave, for slices of sw columns
+        const auto chunk_rows = [&](int w, int64_t nb) {
+            const int64_t per_sm = (nb + sm_count() - 1) / sm_count();
+            const size_t meta = StreamLayout(a.W, a.R, a.G, w, es, is, 0).total;
+            const size_t block_budget = smem_per_sm() / (size_t)per_sm;
+            const size_t reserve = smem_reserved_per_block();
+            const size_t stage_row = (size_t)kStreamStages * w * es;
+            if (block_budget <= meta + reserve) return kStreamRowsMin;
             const int64_t fit = (int64_t)((block_budget - meta - reserve) / stage_row);
             const int most = std::min(kStreamRowsMax, std::max(maxwr, kStreamRowsMin));
-            a.stream_rows = (int)std::max<int64_t>(kStreamRowsMin, std::min<int64_t>(fit, most));
+            return (int)std::max<int64_t>(kStreamRowsMin, std::min<int64_t>(fit, most));
+        };
+        a.stream_rows = chunk_rows(sw, blocks);
+        // Whole rows of up to 1 KiB instead, when that keeps as many SMs busy and gives a taller
+        // chunk: the rows in flight per row of work grow with the chunk height (e.g. 256 streams of
+        // 1 KiB rows: 256 blocks with 24-row chunks instead of 512 blocks of half rows with 19).
+        const int wide = std::min(full, 1024 / es) / q * q;
+        if (wide > sw && a.hd <= wide) {
+            const int64_t nb = a.n_streams;
+            const int64_t busy = std::min<int64_t>(blocks, sm_count()), busy_wide = std::min<int64_t>(nb, sm_count());
+            const int ch = chunk_rows(wide, nb);
+            if (busy_wide >= busy && ch > a.stream_rows) {
+                sw = wide;
+                a.slice_cols = sw;
+                a.n_slices = 1;
+                a.stream_rows = ch;
+            }
         }
     }
+    const int64_t blocks_final = a.n_streams * a.n_slices;
     const int threads = ((sw + cpt - 1) / cpt + 31) / 32 * 32;
     const int path = !vec ? kSimt : streamed ? kStream : kStaged;
     const size_t smem = path == kStaged   ? VecLayout(a.W, a.R, a.G, sw, es, is).total
                         : path == kStream ? StreamLayout(a.W, a.R, a.G, sw, es, is, a.stream_rows).total
                                           : SimtLayout(a.W, a.R, sw, es).total;
 
-    const dim3 grid((unsigned)blocks), block((unsigned)threads);
+    const dim3 grid((unsigned)blocks_final), block((unsigned)threads);
     if (bank_dtype == SDM_BF16) {
         return idx_dtype == SDM_I32 ? launch_typed<uint16_t, int32_t>(path, a, grid, block, smem, stream)
                                     : launch_typed<uint16_t, int64_t>(path, a, grid, block, smem, stream);
