@@ -558,6 +558,43 @@ def plan_slabs(dev, slab: int = 256) -> dict:
     return res
 
 
+def kpos_gather(dev, peak: float) -> dict:
+    """The gather workload with a compact snapshot (sdm_gather_kpos) in place of the stash: operand
+    0's rows are stored once per chunk, at the first position of each distinct row among the
+    chunk's sorted entries (kpos, prepared here on the device before timing)."""
+    from decode_state_gb300 import sdm
+
+    wl = workloads.C4
+    g = workloads.make_gather_inputs(wl, device=dev)
+    idx0 = g["ops"][0][0]
+    W0, n_chunks = idx0.shape[1], wl.tokens // wl.chunk
+    ent = idx0.view(n_chunks, wl.chunk * W0)
+    srt, order = ent.sort(dim=1, stable=True)
+    first = torch.ones_like(srt, dtype=torch.bool)
+    first[:, 1:] = srt[:, 1:] != srt[:, :-1]
+    pos = torch.arange(srt.shape[1], device=dev).expand_as(srt)
+    first_pos = torch.cummax(torch.where(first, pos, torch.zeros_like(pos)), dim=1).values
+    kpos = torch.empty_like(srt).scatter_(1, order, torch.where(first, first_pos, torch.full_like(pos, -1)))
+    kpos = kpos.view(wl.tokens, W0).to(torch.int32)
+    compact = torch.zeros((n_chunks, wl.chunk * W0, wl.hd), dtype=workloads.BANK_DTYPES[wl.bank_dtype], device=dev)
+    outs = [torch.empty((wl.tokens, wl.hd), device=dev) for _ in wl.widths]
+    live = (torch.arange(wl.tokens, device=dev) % wl.chunk) < g["chunk_valid"].repeat_interleave(wl.chunk)
+    es = 2 if wl.bank_dtype == "bf16" else 4
+    written = int(((kpos >= 0) & live[:, None]).sum().item())
+    nbytes = (int(live.sum().item()) * sum(wl.widths) * wl.hd * es + written * wl.hd * es
+              + wl.tokens * len(wl.widths) * wl.hd * 4)
+
+    def step():
+        sdm.gather(g["bank"], g["ops"], chunk=wl.chunk, chunk_valid=g["chunk_valid"], kpos=kpos, compact=compact,
+                   outs=outs)
+
+    ms = _time_calls(step, 20)
+    gbs = nbytes / (ms / 1e3) / 1e9
+    return {"workload": wl.name + " with a compact snapshot", "unit_per_s": wl.tokens / (ms / 1e3), "unit": "tokens/s",
+            "ms_per_step": ms, "compact_rows_written": written, "algorithmic_bytes": nbytes, "effective_gbs": gbs,
+            "frac_of_hbm_peak": gbs / peak}
+
+
 # ---------------------------------------------------------------- reference arm (the oracle)
 
 
@@ -622,6 +659,9 @@ def main():
             res["other_workloads"] = extras(args, torch.device("cuda", r.local_rank), r, res["roofline"]["peak"],
                                             res["config"]["workload"])
             res["other_workloads"]["gather_plan_slabs"] = plan_slabs(torch.device("cuda", r.local_rank))
+            torch.cuda.empty_cache()
+            res["other_workloads"]["gather_kpos"] = kpos_gather(torch.device("cuda", r.local_rank),
+                                                                res["roofline"]["peak"])
             torch.cuda.empty_cache()
         if r.is_root:
             print(json.dumps(res), flush=True)
