@@ -460,20 +460,22 @@ __global__ void __launch_bounds__(kMaxThreads, 2) decode_vec_kernel(const Decode
 // 1 KiB), the rows stream through a ring of NS chunk buffers of CH rows each instead of being
 // staged all at once: the write rows pass twice (retrieve, then decay-and-write; the second pass
 // is served mostly by L2) and the read rows once. Chunks are consumed in ascending row order, so
-// every sum keeps the order and the bits of the staged path. CH is chosen at launch: the largest
-// chunk (kStreamRowsMin..kStreamRowsMax rows) whose ring still lets every block of the grid be
-// resident at once; larger chunks put more rows in flight and take fewer barriers per pass.
+// every sum keeps the order and the bits of the staged path. NS and CH are chosen at launch: CH
+// is the largest chunk (kStreamRowsMin..kStreamRowsMax rows) whose ring still lets every block of
+// the grid be resident at once (larger chunks put more rows in flight and take fewer barriers per
+// pass), with NS = 3 when that allows chunks of kTallChunk rows or more, else NS = 4.
 
 constexpr int kStreamRowsMin = 16;  // rows per chunk, at least
 constexpr int kStreamRowsMax = 32;  // and at most
-constexpr int kStreamStages = 4;    // chunk buffers in the ring
+constexpr int kTallChunk = 24;      // three stages suffice from this chunk height on
 
 struct StreamLayout {
     VecLayout meta;  // the metadata of the staged layout, with no row area
     size_t ring, total;
-    __host__ __device__ StreamLayout(int W, int R, int G, int sw, int es, int is, int ch) : meta(W, R, G, 0, es, is) {
+    __host__ __device__ StreamLayout(int W, int R, int G, int sw, int es, int is, int ch, int ns)
+        : meta(W, R, G, 0, es, is) {
         ring = align_up(meta.total, 128);
-        total = ring + (size_t)kStreamStages * ch * sw * es;
+        total = ring + (size_t)ns * ch * sw * es;
     }
 };
 
@@ -484,17 +486,16 @@ __device__ __forceinline__ void ldgsts_chunk(unsigned char* dst, const unsigned 
     ldgsts_rows<E>(reinterpret_cast<E*>(dst), bank, off + r0, n, sw, row_bytes);
 }
 
-template <typename E, typename I>
+template <typename E, typename I, int NS>
 __global__ void __launch_bounds__(kMaxThreads, 1) decode_stream_kernel(const DecodeArgs a, int early_trigger) {
     using P = Pair<E>;
     using PT = typename P::T;
     constexpr int ES = sizeof(E);
-    constexpr int NS = kStreamStages;
     const int CH = a.stream_rows;
     extern __shared__ __align__(128) unsigned char smem[];
 
     const int W = a.W, R = a.R, G = a.G, hd = a.hd, sw = a.slice_cols;
-    const StreamLayout SL(W, R, G, sw, ES, (int)sizeof(I), CH);
+    const StreamLayout SL(W, R, G, sw, ES, (int)sizeof(I), CH, NS);
     const VecLayout& L = SL.meta;
     unsigned char* ring = smem + SL.ring;
     const size_t stage_bytes = (size_t)CH * sw * ES;
@@ -725,7 +726,8 @@ enum Path { kSimt = 0, kStaged = 1, kStream = 2 };
 template <typename E, typename I>
 int launch_typed(int path, const DecodeArgs& a, dim3 grid, dim3 block, size_t smem, cudaStream_t stream) {
     const auto kernel = path == kStaged   ? (a.piece_write ? decode_vec_kernel<E, I, true> : decode_vec_kernel<E, I, false>)
-                        : path == kStream ? decode_stream_kernel<E, I>
+                        : path == kStream ? (a.stream_stages == 3 ? decode_stream_kernel<E, I, 3>
+                                                                  : decode_stream_kernel<E, I, 4>)
                                           : decode_simt_kernel<E, I>;
     const int early = fits_one_wave(kernel, grid.x, (int)block.x, smem) ? 1 : 0;
     return launch_pdl(kernel, grid, block, smem, stream, a, early);
@@ -774,41 +776,56 @@ int launch_decode(const DecodeArgs& a0, int bank_dtype, int idx_dtype, cudaStrea
     // (bandwidth-bound), not when a few blocks per SM wait on latency
     a.piece_write = blocks >= 4LL * sm_count() ? 1 : 0;
     a.stream_rows = kStreamRowsMin;
+    a.stream_stages = 4;
     if (streamed) {
-        // the largest chunk that keeps the whole grid resident in one wave, for slices of sw columns
-        const auto chunk_rows = [&](int w, int64_t nb) {
+        // the largest chunk that keeps the whole grid resident in one wave, for slices of w columns
+        // and a ring of ns chunks
+        const auto chunk_rows = [&](int w, int64_t nb, int ns) {
             const int64_t per_sm = (nb + sm_count() - 1) / sm_count();
-            const size_t meta = StreamLayout(a.W, a.R, a.G, w, es, is, 0).total;
+            const size_t meta = StreamLayout(a.W, a.R, a.G, w, es, is, 0, ns).total;
             const size_t block_budget = smem_per_sm() / (size_t)per_sm;
             const size_t reserve = smem_reserved_per_block();
-            const size_t stage_row = (size_t)kStreamStages * w * es;
+            const size_t stage_row = (size_t)ns * w * es;
             if (block_budget <= meta + reserve) return kStreamRowsMin;
             const int64_t fit = (int64_t)((block_budget - meta - reserve) / stage_row);
             const int most = std::min(kStreamRowsMax, std::max(maxwr, kStreamRowsMin));
             return (int)std::max<int64_t>(kStreamRowsMin, std::min<int64_t>(fit, most));
         };
-        a.stream_rows = chunk_rows(sw, blocks);
-        // Whole rows of up to 1 KiB instead, when that keeps as many SMs busy and gives a taller
-        // chunk: the rows in flight per row of work grow with the chunk height (e.g. 256 streams of
-        // 1 KiB rows: 256 blocks with 24-row chunks instead of 512 blocks of half rows with 19).
+        // The slices as chosen above, or whole rows of up to 1 KiB instead when that keeps as many
+        // SMs busy and gives a taller chunk: the rows in flight per row of work grow with the
+        // chunk height (e.g. 256 streams of 1 KiB rows: 256 blocks with 32-row chunks instead of
+        // 512 blocks of half rows with 25).
         const int wide = std::min(full, 1024 / es) / q * q;
-        if (wide > sw && a.hd <= wide) {
-            const int64_t nb = a.n_streams;
-            const int64_t busy = std::min<int64_t>(blocks, sm_count()), busy_wide = std::min<int64_t>(nb, sm_count());
-            const int ch = chunk_rows(wide, nb);
-            if (busy_wide >= busy && ch > a.stream_rows) {
-                sw = wide;
-                a.slice_cols = sw;
-                a.n_slices = 1;
-                a.stream_rows = ch;
+        const auto geometry = [&](int ns, int& w, int& ch) {
+            w = sw;
+            ch = chunk_rows(sw, blocks, ns);
+            if (wide > sw && a.hd <= wide) {
+                const int64_t busy = std::min<int64_t>(blocks, sm_count());
+                const int64_t busy_wide = std::min<int64_t>(a.n_streams, sm_count());
+                const int chw = chunk_rows(wide, a.n_streams, ns);
+                if (busy_wide >= busy && chw > ch) {
+                    w = wide;
+                    ch = chw;
+                }
             }
+        };
+        int w = sw, ch = kStreamRowsMin;
+        geometry(3, w, ch);
+        if (ch >= kTallChunk) {
+            a.stream_stages = 3;
+        } else {
+            geometry(4, w, ch);
         }
+        sw = w;
+        a.slice_cols = sw;
+        a.n_slices = (a.hd + sw - 1) / sw;
+        a.stream_rows = ch;
     }
     const int64_t blocks_final = a.n_streams * a.n_slices;
     const int threads = ((sw + cpt - 1) / cpt + 31) / 32 * 32;
     const int path = !vec ? kSimt : streamed ? kStream : kStaged;
     const size_t smem = path == kStaged   ? VecLayout(a.W, a.R, a.G, sw, es, is).total
-                        : path == kStream ? StreamLayout(a.W, a.R, a.G, sw, es, is, a.stream_rows).total
+                        : path == kStream ? StreamLayout(a.W, a.R, a.G, sw, es, is, a.stream_rows, a.stream_stages).total
                                           : SimtLayout(a.W, a.R, sw, es).total;
 
     const dim3 grid((unsigned)blocks_final), block((unsigned)threads);

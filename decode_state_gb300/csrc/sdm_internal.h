@@ -21,7 +21,8 @@ struct DecodeArgs {
     int hd, W, R, G, T;
     int slice_cols;   // columns one block owns (the last slice may be narrower)
     int n_slices;     // ceil(hd / slice_cols)
-    int stream_rows;  // rows per ring chunk of the streaming path
+    int stream_rows;    // rows per ring chunk of the streaming path
+    int stream_stages;  // chunk buffers in its ring (3 or 4)
     int piece_write;  // staged path: decay-and-write by 16-byte pieces (many blocks per SM)
 };
 
