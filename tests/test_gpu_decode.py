@@ -254,3 +254,19 @@ def test_gather_after_decode_sees_its_writes():
     torch.cuda.synchronize()
     assert torch.equal(stash[:, 0].view(torch.int16), x["bank"][idx[:, 0].long()].view(torch.int16))
     assert torch.equal(outs[0], x["bank"][idx[:, 0].long()].float())
+
+
+def test_streamed_decode_many_streams_matches_oracle():
+    """Wide rows across many streams: 512 streams of 1 KiB float32 rows with W = R = 256 fill more
+    than one wave of blocks, so the streaming path runs 16-row chunks in a four-stage ring (smaller
+    grids take three stages); compared with the oracle on every stream."""
+    wl = workloads.DecodeWorkload("wide_many", "f32", 512, 256, 300, 256, 256, 1, 2, "i64", 1 / 16, bank_std=0.5,
+                                  seed=9)
+    x = workloads.make_decode_inputs(wl, device=DEV)
+    bank_ref = to_np(x["bank"])
+    ref = oracle.decode_seq(bank_ref, *(to_np(x[k]) for k in DECODE_KEYS))
+    out = sdm.decode_seq(x["bank"], *(x[k] for k in DECODE_KEYS))
+    torch.cuda.synchronize()
+    assert_close(to_np(out), ref, "f32", "readings")
+    assert_close(to_np(x["bank"]), bank_ref, "f32", "bank")
+    assert sdm.device_status() == 0
