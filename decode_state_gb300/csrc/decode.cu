@@ -337,30 +337,30 @@ __global__ void __launch_bounds__(kMaxThreads, 2) decode_vec_kernel(const Decode
             const uint64_t delta = f2(dl, dh);
             if (by_piece) {
                 reinterpret_cast<uint64_t*>(smem + L.dlt)[tid] = delta;
-            } else {
-            unsigned char* bj = bank + jb;
-            w = 0;
+            } else {  // each thread writes its own pair of every row
+                unsigned char* bj = bank + jb;
+                w = 0;
 #pragma unroll 2
-            for (; w + 2 <= W; w += 2) {
-                const uint64_t x0 = P::widen(rp[w * pstride]), x1 = P::widen(rp[(w + 1) * pstride]);
-                const ulonglong2 k2 = *reinterpret_cast<const ulonglong2*>(kv2 + w);
-                const longlong2 o2 = *reinterpret_cast<const longlong2*>(koff + w);
-                uint64_t d0 = dsh, d1 = dsh;
-                if (G != 1) {
-                    const ulonglong2 dd = *reinterpret_cast<const ulonglong2*>(dw2 + w);
-                    d0 = dd.x;
-                    d1 = dd.y;
+                for (; w + 2 <= W; w += 2) {
+                    const uint64_t x0 = P::widen(rp[w * pstride]), x1 = P::widen(rp[(w + 1) * pstride]);
+                    const ulonglong2 k2 = *reinterpret_cast<const ulonglong2*>(kv2 + w);
+                    const longlong2 o2 = *reinterpret_cast<const longlong2*>(koff + w);
+                    uint64_t d0 = dsh, d1 = dsh;
+                    if (G != 1) {
+                        const ulonglong2 dd = *reinterpret_cast<const ulonglong2*>(dw2 + w);
+                        d0 = dd.x;
+                        d1 = dd.y;
+                    }
+                    const uint64_t y0 = ffma2(k2.x, delta, fmul2(x0, d0));
+                    const uint64_t y1 = ffma2(k2.y, delta, fmul2(x1, d1));
+                    *reinterpret_cast<PT*>(bj + o2.x) = P::narrow(y0);
+                    *reinterpret_cast<PT*>(bj + o2.y) = P::narrow(y1);
                 }
-                const uint64_t y0 = ffma2(k2.x, delta, fmul2(x0, d0));
-                const uint64_t y1 = ffma2(k2.y, delta, fmul2(x1, d1));
-                *reinterpret_cast<PT*>(bj + o2.x) = P::narrow(y0);
-                *reinterpret_cast<PT*>(bj + o2.y) = P::narrow(y1);
-            }
-            for (; w < W; ++w) {
-                const uint64_t x = P::widen(rp[w * pstride]);
-                const uint64_t y = ffma2(kv2[w], delta, fmul2(x, G == 1 ? dsh : dw2[w]));
-                *reinterpret_cast<PT*>(bj + koff[w]) = P::narrow(y);
-            }
+                for (; w < W; ++w) {
+                    const uint64_t x = P::widen(rp[w * pstride]);
+                    const uint64_t y = ffma2(kv2[w], delta, fmul2(x, G == 1 ? dsh : dw2[w]));
+                    *reinterpret_cast<PT*>(bj + koff[w]) = P::narrow(y);
+                }
             }
         }
         if (by_piece) {
