@@ -270,3 +270,29 @@ def test_streamed_decode_many_streams_matches_oracle():
     assert_close(to_np(out), ref, "f32", "readings")
     assert_close(to_np(x["bank"]), bank_ref, "f32", "bank")
     assert sdm.device_status() == 0
+
+
+def test_concurrent_calls_on_two_streams_match_sequential():
+    """The library keeps no state between calls: a decode of one bank and a gather of another,
+    launched on two CUDA streams without synchronising between them, give the same bits as the same
+    calls run one after the other."""
+    wd = workloads.C2.scaled(n_streams=256, T=16)
+    wg = workloads.C4.scaled(tokens=8192)
+    xd = workloads.make_decode_inputs(wd, device=DEV)
+    g = workloads.make_gather_inputs(wg, device=DEV)
+    bank0 = xd["bank"].clone()
+    ref_out = sdm.decode_seq(xd["bank"], *(xd[k] for k in DECODE_KEYS))
+    ref_g, ref_stash = sdm.gather(g["bank"], g["ops"], chunk=wg.chunk, chunk_valid=g["chunk_valid"])
+    torch.cuda.synchronize()
+    ref_bank = xd["bank"].clone()
+    xd["bank"].copy_(bank0)
+    torch.cuda.synchronize()
+    s1, s2 = torch.cuda.Stream(DEV), torch.cuda.Stream(DEV)
+    with torch.cuda.stream(s1):
+        out = sdm.decode_seq(xd["bank"], *(xd[k] for k in DECODE_KEYS), stream=s1)
+    with torch.cuda.stream(s2):
+        outs, stash = sdm.gather(g["bank"], g["ops"], chunk=wg.chunk, chunk_valid=g["chunk_valid"], stream=s2)
+    torch.cuda.synchronize()
+    assert bits_equal(to_np(out), to_np(ref_out)) and bits_equal(to_np(xd["bank"]), to_np(ref_bank))
+    assert all(bits_equal(to_np(a), to_np(b)) for a, b in zip(outs, ref_g))
+    assert bits_equal(to_np(stash), to_np(ref_stash))
