@@ -519,6 +519,20 @@ def extras(args, dev, r: sdist.Rank, peak: float, skip: str):
             item.update({"graph_unit_per_s": case.units / (gms / 1e3), "graph_ms_per_step": gms,
                          "graph_us_per_launch": gms * 1e3 / case.launches})
             del graph
+            # the same launches eagerly through a plan (checked once, pointers precomputed)
+            from decode_state_gb300 import sdm
+
+            plan = sdm.DecodeStepPlan(case.x["bank"], {k: case.x[k] for k in DECODE_KEYS}, out=case.out,
+                                      stream=torch.cuda.current_stream(dev))
+
+            def plan_steps():
+                for t in range(case.wl.T):
+                    plan.launch(t)
+
+            pms = _time_calls(plan_steps, reps)
+            item.update({"plan_unit_per_s": case.units / (pms / 1e3), "plan_ms_per_step": pms,
+                         "plan_us_per_launch": pms * 1e3 / case.launches})
+            del plan
         res[name] = item
         del case
         torch.cuda.empty_cache()

@@ -246,6 +246,41 @@ def gather(bank, ops, *, chunk: int, valid: int | None = None, chunk_valid=None,
     return outs, stash
 
 
+class DecodeStepPlan:
+    """Single-token decode steps over fixed device buffers, checked once (sdm_decode_step).
+
+    ``inputs`` maps the names of ``DECODE_KEYS`` to time-major device tensors [T, S, .] (beta
+    [T, S]) that the caller fills; ``launch(t)`` runs sdm_decode_step on step t's slabs and writes
+    the readings into ``out[t]`` ([T, S, hd], allocated when not given). Shapes, dtypes, devices
+    and every step's pointers are settled here, so a launch is one foreign call. The plan keeps
+    references to its tensors; they must not be resized or reallocated in place.
+    """
+
+    DECODE_KEYS = ("k_idx", "k_val", "v", "beta", "g", "q_idx", "q_val")
+
+    def __init__(self, bank, inputs: dict, out=None, stream=None):
+        T = inputs["k_idx"].shape[0]
+        if out is None:
+            out = torch.empty((T, inputs["k_idx"].shape[1], bank.shape[1]), dtype=bank.dtype, device=bank.device)
+        args = [inputs[k] for k in self.DECODE_KEYS]
+        self.out, _, hd, W, R, G, _ = _decode_args(bank, *args, out, (T, inputs["k_idx"].shape[1]), stream)
+        S = inputs["k_idx"].shape[1]
+        self._tail = (S, hd, W, R, G, _BANK_CODES[bank.dtype], _IDX_CODES[inputs["k_idx"].dtype])
+        self._steps = [(bank.data_ptr(), *(a[t].data_ptr() for a in args), self.out[t].data_ptr()) for t in range(T)]
+        self._fn = library().sdm_decode_step
+        self._stream = _stream_handle(stream, bank.device) if stream is not None else None
+        self._keep = (bank, inputs)
+        self.device, self.T = bank.device, T
+
+    def launch(self, t: int, stream=None) -> torch.Tensor:
+        """Step t (0 <= t < T) on the bank; returns the readings out[t]."""
+        st = self._stream if stream is None and self._stream is not None else _stream_handle(stream, self.device)
+        rc = self._fn(*self._steps[t], *self._tail, st)
+        if rc != 0:
+            _check("sdm_decode_step", rc)
+        return self.out[t]
+
+
 class GatherPlan:
     """A checked no-stash gather launch replayed per slab (sdm_gather_plan_init / _launch).
 

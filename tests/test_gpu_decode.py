@@ -239,6 +239,28 @@ def test_step_graph_matches_eager_steps():
     assert torch.equal(bank_g.view(torch.int16), x["bank"].view(torch.int16))
 
 
+def test_decode_step_plan_matches_eager_steps():
+    """T single-token launches through a DecodeStepPlan (checked once, pointers precomputed) equal
+    the same launches through decode_step, on the default stream and on a given one."""
+    wl = _wl("f32", "i32", 16, 256, 96, 24, 40, 1, 5, seed=13)
+    x = workloads.make_decode_inputs(wl, device=DEV)
+    bank_p = x["bank"].clone()
+    plan = sdm.DecodeStepPlan(bank_p, {k: x[k] for k in DECODE_KEYS})
+    for t in range(wl.T):
+        if t == 2:
+            side = torch.cuda.Stream(DEV)
+            side.wait_stream(torch.cuda.current_stream(DEV))
+            with torch.cuda.stream(side):
+                plan.launch(t, stream=side)
+            torch.cuda.current_stream(DEV).wait_stream(side)
+        else:
+            plan.launch(t)
+    eager = [sdm.decode_step(x["bank"], *(x[k][t] for k in DECODE_KEYS)) for t in range(wl.T)]
+    torch.cuda.synchronize()
+    assert torch.equal(plan.out.view(torch.int32), torch.stack(eager).view(torch.int32))
+    assert torch.equal(bank_p.view(torch.int32), x["bank"].view(torch.int32))
+
+
 def test_gather_after_decode_sees_its_writes():
     """A gather launched right after a decode on the same stream (no host synchronisation) reads
     the rows the decode wrote: the overlapped launch waits for its predecessor before reading."""
