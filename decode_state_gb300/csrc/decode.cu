@@ -624,6 +624,131 @@ __global__ void __launch_bounds__(kMaxThreads, 1) decode_stream_kernel(const Dec
     }
 }
 
+// The streaming path for float32 banks with one column per thread, for slices of up to 128
+// columns: the same ring, metadata and order of operations as decode_stream_kernel, but scalar
+// float32 chains (each lane of a paired op is an independent round-to-nearest op, so the bits are
+// the same) and twice the warps to cover the chains' latency.
+template <typename I, int NS>
+__global__ void __launch_bounds__(kMaxThreads, 1) decode_stream1_kernel(const DecodeArgs a, int early_trigger) {
+    constexpr int ES = 4;
+    const int CH = a.stream_rows;
+    extern __shared__ __align__(128) unsigned char smem[];
+
+    const int W = a.W, R = a.R, G = a.G, hd = a.hd, sw = a.slice_cols;
+    const StreamLayout SL(W, R, G, sw, ES, (int)sizeof(I), CH, NS);
+    const VecLayout& L = SL.meta;
+    unsigned char* ring = smem + SL.ring;
+    const size_t stage_bytes = (size_t)CH * sw * ES;
+    const int64_t* koff = reinterpret_cast<const int64_t*>(smem + L.koff);
+    const int64_t* qoff = reinterpret_cast<const int64_t*>(smem + L.qoff);
+    const uint64_t* aw2 = reinterpret_cast<const uint64_t*>(smem + L.aw2);
+    const uint64_t* kv2 = reinterpret_cast<const uint64_t*>(smem + L.kv2);
+    const uint64_t* dw2 = reinterpret_cast<const uint64_t*>(smem + L.dw2);
+    const uint64_t* qv2 = reinterpret_cast<const uint64_t*>(smem + L.qv2);
+
+    const int tid = threadIdx.x;
+    const int64_t s = blockIdx.x / a.n_slices;
+    const int c0 = (int)(blockIdx.x % a.n_slices) * sw;
+    const int ncols = min(sw, hd - c0);
+    const int j = tid;
+    const bool active = j < ncols;
+    const uint32_t row_bytes = (uint32_t)ncols * ES;
+    unsigned char* bank = static_cast<unsigned char*>(a.bank);
+    float* out = static_cast<float*>(a.out);
+    const int64_t jb = (int64_t)j * ES;
+    const int nk = (W + CH - 1) / CH, nq = (R + CH - 1) / CH;
+    const auto at = [&](int st, int r) -> float {
+        return reinterpret_cast<const float*>(ring + st * stage_bytes)[r * sw + tid];
+    };
+
+    grid_dependency_wait();
+    if (early_trigger) grid_launch_dependents();
+    prefetch_meta<I>(a, s, L, smem);  // token 0
+    cp_async_wait_all();
+    __syncthreads();
+    if (G == 1 && tid == 0)
+        *reinterpret_cast<float*>(smem + L.dnext) = (float)exp((double)*reinterpret_cast<const float*>(smem + L.raw_g));
+    __syncthreads();
+    derive_meta<float, I>(a, c0, L, smem);
+    __syncthreads();
+
+    for (int t = 0; t < a.T; ++t) {
+        const int64_t ts = (int64_t)t * a.n_streams + s;
+        const float vr = active ? __ldg(a.v + ts * hd + c0 + j) : 0.0f;
+        const float beta = *reinterpret_cast<const float*>(smem + L.beta);
+        const float dsh = f2lo(dw2[0]);
+
+        float acc = 0.0f, delta = 0.0f;
+        const int jobs = 2 * nk;
+        for (int q = 0; q < NS - 1; ++q) {
+            if (q < jobs) {
+                const int c = q % nk;
+                ldgsts_chunk<float>(ring + (q % NS) * stage_bytes, bank, koff, c * CH, min(CH, W - c * CH), sw, row_bytes);
+            } else {
+                cp_async_commit();
+            }
+        }
+        for (int q = 0; q < jobs; ++q) {
+            const int qn = q + NS - 1;
+            if (qn < jobs) {
+                const int c = qn % nk;
+                ldgsts_chunk<float>(ring + (qn % NS) * stage_bytes, bank, koff, c * CH, min(CH, W - c * CH), sw, row_bytes);
+            } else {
+                cp_async_commit();
+            }
+            asm volatile("cp.async.wait_group %0;" ::"n"(NS - 1) : "memory");
+            __syncthreads();
+            const int st = q % NS, c = q % nk, r0 = c * CH, n = min(CH, W - r0);
+            if (active) {
+                if (q < nk) {
+                    for (int r = 0; r < n; ++r) acc = fmaf(f2lo(aw2[r0 + r]), at(st, r), acc);
+                } else {
+                    if (q == nk) delta = __fmul_rn(beta, __fsub_rn(vr, acc));
+                    for (int r = 0; r < n; ++r) {
+                        const int w = r0 + r;
+                        const float y = fmaf(f2lo(kv2[w]), delta, __fmul_rn(at(st, r), G == 1 ? dsh : f2lo(dw2[w])));
+                        *reinterpret_cast<float*>(bank + koff[w] + jb) = y;
+                    }
+                }
+            }
+            __syncthreads();
+        }
+
+        const bool more = t + 1 < a.T;
+        if (more) {
+            prefetch_meta<I>(a, ts + a.n_streams, L, smem);
+            if (G == 1 && tid == 0)
+                *reinterpret_cast<float*>(smem + L.dnext) = (float)exp((double)__ldg(a.g + ts + a.n_streams));
+        }
+        float racc = 0.0f;
+        for (int q = 0; q < NS - 1; ++q) {
+            if (q < nq)
+                ldgsts_chunk<float>(ring + (q % NS) * stage_bytes, bank, qoff, q * CH, min(CH, R - q * CH), sw, row_bytes);
+            else
+                cp_async_commit();
+        }
+        for (int q = 0; q < nq; ++q) {
+            const int qn = q + NS - 1;
+            if (qn < nq)
+                ldgsts_chunk<float>(ring + (qn % NS) * stage_bytes, bank, qoff, qn * CH, min(CH, R - qn * CH), sw, row_bytes);
+            else
+                cp_async_commit();
+            asm volatile("cp.async.wait_group %0;" ::"n"(NS - 1) : "memory");
+            __syncthreads();
+            const int st = q % NS, r0 = q * CH, n = min(CH, R - r0);
+            if (active)
+                for (int r = 0; r < n; ++r) racc = fmaf(f2lo(qv2[r0 + r]), at(st, r), racc);
+            __syncthreads();
+        }
+        if (active) out[ts * hd + c0 + j] = racc;
+
+        cp_async_wait_all();
+        __syncthreads();
+        if (more) derive_meta<float, I>(a, c0, L, smem);
+        __syncthreads();
+    }
+}
+
 // ---------------------------------------------------------------- plain-load path
 
 struct SimtLayout {
@@ -723,11 +848,19 @@ __global__ void __launch_bounds__(kMaxThreads) decode_simt_kernel(const DecodeAr
 
 enum Path { kSimt = 0, kStaged = 1, kStream = 2 };
 
+template <typename I, int NS>
+auto stream1_kernel() {
+    return decode_stream1_kernel<I, NS>;
+}
+
 template <typename E, typename I>
-int launch_typed(int path, const DecodeArgs& a, dim3 grid, dim3 block, size_t smem, cudaStream_t stream) {
+int launch_typed(int path, bool scalar, const DecodeArgs& a, dim3 grid, dim3 block, size_t smem, cudaStream_t stream) {
     const auto kernel = path == kStaged   ? (a.piece_write ? decode_vec_kernel<E, I, true> : decode_vec_kernel<E, I, false>)
-                        : path == kStream ? (a.stream_stages == 3 ? decode_stream_kernel<E, I, 3>
-                                                                  : decode_stream_kernel<E, I, 4>)
+                        : path == kStream
+                            ? ((sizeof(E) == 4 && scalar)  // a column per thread
+                                   ? (a.stream_stages == 3 ? stream1_kernel<I, 3>() : stream1_kernel<I, 4>())
+                                   : (a.stream_stages == 3 ? decode_stream_kernel<E, I, 3>
+                                                           : decode_stream_kernel<E, I, 4>))
                                           : decode_simt_kernel<E, I>;
     const int early = fits_one_wave(kernel, grid.x, (int)block.x, smem) ? 1 : 0;
     return launch_pdl(kernel, grid, block, smem, stream, a, early);
@@ -822,19 +955,23 @@ int launch_decode(const DecodeArgs& a0, int bank_dtype, int idx_dtype, cudaStrea
         a.stream_rows = ch;
     }
     const int64_t blocks_final = a.n_streams * a.n_slices;
-    const int threads = ((sw + cpt - 1) / cpt + 31) / 32 * 32;
     const int path = !vec ? kSimt : streamed ? kStream : kStaged;
+    // float32 streaming over slices of up to 128 columns: one column per thread (scalar chains,
+    // twice the warps); wider slices keep column pairs (blocks of 256 threads measured slower)
+    const bool scalar = path == kStream && es == 4 && sw <= 128;
+    const int tcols = scalar ? 1 : cpt;
+    const int threads = ((sw + tcols - 1) / tcols + 31) / 32 * 32;
     const size_t smem = path == kStaged   ? VecLayout(a.W, a.R, a.G, sw, es, is).total
                         : path == kStream ? StreamLayout(a.W, a.R, a.G, sw, es, is, a.stream_rows, a.stream_stages).total
                                           : SimtLayout(a.W, a.R, sw, es).total;
 
     const dim3 grid((unsigned)blocks_final), block((unsigned)threads);
     if (bank_dtype == SDM_BF16) {
-        return idx_dtype == SDM_I32 ? launch_typed<uint16_t, int32_t>(path, a, grid, block, smem, stream)
-                                    : launch_typed<uint16_t, int64_t>(path, a, grid, block, smem, stream);
+        return idx_dtype == SDM_I32 ? launch_typed<uint16_t, int32_t>(path, scalar, a, grid, block, smem, stream)
+                                    : launch_typed<uint16_t, int64_t>(path, scalar, a, grid, block, smem, stream);
     }
-    return idx_dtype == SDM_I32 ? launch_typed<float, int32_t>(path, a, grid, block, smem, stream)
-                                : launch_typed<float, int64_t>(path, a, grid, block, smem, stream);
+    return idx_dtype == SDM_I32 ? launch_typed<float, int32_t>(path, scalar, a, grid, block, smem, stream)
+                                : launch_typed<float, int64_t>(path, scalar, a, grid, block, smem, stream);
 }
 
 int decode_status(unsigned int* word, bool clear) {
