@@ -455,6 +455,170 @@ __global__ void __launch_bounds__(kMaxThreads, 2) decode_vec_kernel(const Decode
 }
 
 
+// acc + q * x with q the bf16 in the high half of the float32 pattern qbits and x a bf16 element
+__device__ __forceinline__ float fma_bf16(float acc, uint32_t qbits, uint16_t x) {
+    asm("{\n\t.reg .b16 ql, qh;\n\tmov.b32 {ql, qh}, %1;\n\tfma.rn.f32.bf16 %0, qh, %2, %0;\n\t}"
+        : "+f"(acc)
+        : "r"(qbits), "h"(x));
+    return acc;
+}
+
+// The staged path for bf16 slices of up to 64 columns with one column per thread: the same
+// staging, order of operations and write-back as decode_vec_kernel, scalar chains (each lane of a
+// paired op is an independent round-to-nearest op, so the bits are the same) and twice the warps.
+template <typename I, bool PIECE>
+__global__ void __launch_bounds__(128, 7) decode_vec1_kernel(const DecodeArgs a, int early_trigger) {
+    using E = uint16_t;
+    using P = Pair<E>;
+    constexpr int ES = 2;
+    extern __shared__ __align__(128) unsigned char smem[];
+
+    const int W = a.W, R = a.R, G = a.G, hd = a.hd, sw = a.slice_cols;
+    const VecLayout L(W, R, G, sw, ES, (int)sizeof(I));
+    E* rows = reinterpret_cast<E*>(smem + L.rows);
+    const int64_t* koff = reinterpret_cast<const int64_t*>(smem + L.koff);
+    const int64_t* qoff = reinterpret_cast<const int64_t*>(smem + L.qoff);
+    const uint64_t* aw2 = reinterpret_cast<const uint64_t*>(smem + L.aw2);
+    const uint64_t* kv2 = reinterpret_cast<const uint64_t*>(smem + L.kv2);
+    const uint64_t* dw2 = reinterpret_cast<const uint64_t*>(smem + L.dw2);
+    const uint64_t* qv2 = reinterpret_cast<const uint64_t*>(smem + L.qv2);
+
+    const int tid = threadIdx.x, nt = blockDim.x;
+    const int64_t s = blockIdx.x / a.n_slices;
+    const int c0 = (int)(blockIdx.x % a.n_slices) * sw;
+    const int ncols = min(sw, hd - c0);
+    const int j = tid;
+    const bool active = j < ncols;
+    const uint32_t row_bytes = (uint32_t)ncols * ES;
+    unsigned char* bank = static_cast<unsigned char*>(a.bank);
+    E* out = static_cast<E*>(a.out);
+    const E* rc = rows + tid;  // this thread's element of row 0
+    const int64_t jb = (int64_t)j * ES;
+    const int cpr = (int)(row_bytes >> 4);
+    const bool by_piece = PIECE && a.piece_write && nt % cpr == 0 && nt / cpr <= W;
+
+    grid_dependency_wait();
+    if (early_trigger) grid_launch_dependents();
+    prefetch_meta<I>(a, s, L, smem);  // token 0
+    cp_async_wait_all();
+    __syncthreads();
+    if (G == 1 && tid == 0)
+        *reinterpret_cast<float*>(smem + L.dnext) = (float)exp((double)*reinterpret_cast<const float*>(smem + L.raw_g));
+    __syncthreads();
+    derive_meta<E, I>(a, c0, L, smem);
+    __syncthreads();
+
+    for (int t = 0; t < a.T; ++t) {
+        const int64_t ts = (int64_t)t * a.n_streams + s;
+
+        ldgsts_rows<E>(rows, bank, koff, W, sw, row_bytes);
+        {
+            const int lines = (int)((row_bytes + 127) >> 7);
+            for (int i = tid; i < R * lines; i += nt) {
+                const int r = i / lines, l = i - r * lines;
+                asm volatile("prefetch.global.L2 [%0];" ::"l"(bank + qoff[r] + (int64_t)l * 128));
+            }
+        }
+        const float vr = active ? round_to<E>(__ldg(a.v + ts * hd + c0 + j)) : 0.0f;
+        const float beta = *reinterpret_cast<const float*>(smem + L.beta);
+        const float dsh = f2lo(dw2[0]);
+        const bool more = t + 1 < a.T;
+        if (more) {
+            prefetch_meta<I>(a, ts + a.n_streams, L, smem);
+            if (G == 1 && tid == 0)
+                *reinterpret_cast<float*>(smem + L.dnext) = (float)exp((double)__ldg(a.g + ts + a.n_streams));
+        }
+        if (more)
+            asm volatile("cp.async.wait_group 1;" ::: "memory");
+        else
+            cp_async_wait_all();
+        __syncthreads();
+
+        if (active) {
+            float acc = 0.0f;
+            int w = 0;
+            for (; w + 4 <= W; w += 4) {
+                const E x0 = rc[(w + 0) * sw], x1 = rc[(w + 1) * sw], x2 = rc[(w + 2) * sw], x3 = rc[(w + 3) * sw];
+                const ulonglong2 a01 = *reinterpret_cast<const ulonglong2*>(aw2 + w);
+                const ulonglong2 a23 = *reinterpret_cast<const ulonglong2*>(aw2 + w + 2);
+                acc = fmaf(f2lo(a01.x), to_f32(x0), acc);
+                acc = fmaf(f2lo(a01.y), to_f32(x1), acc);
+                acc = fmaf(f2lo(a23.x), to_f32(x2), acc);
+                acc = fmaf(f2lo(a23.y), to_f32(x3), acc);
+            }
+            for (; w < W; ++w) acc = fmaf(f2lo(aw2[w]), to_f32(rc[w * sw]), acc);
+            const float delta = __fmul_rn(beta, __fsub_rn(vr, acc));
+            if (by_piece) {
+                reinterpret_cast<float*>(smem + L.dlt)[tid] = delta;
+            } else {
+                unsigned char* bj = bank + jb;
+                for (w = 0; w < W; ++w) {
+                    const float y = fmaf(f2lo(kv2[w]), delta, __fmul_rn(to_f32(rc[w * sw]), G == 1 ? dsh : f2lo(dw2[w])));
+                    *reinterpret_cast<E*>(bj + koff[w]) = from_f32<E>(y);
+                }
+            }
+        }
+        if (by_piece) {
+            __syncthreads();
+            constexpr int PP = 16 / (2 * ES);
+            const int k = tid % cpr, ngroups = nt / cpr;
+            const uint64_t d_sh = dw2[0];
+            uint64_t dp[PP];
+#pragma unroll
+            for (int p = 0; p < PP; ++p) dp[p] = reinterpret_cast<const uint64_t*>(smem + L.dlt)[k * PP + p];
+            const unsigned char* src = reinterpret_cast<const unsigned char*>(rows) + k * 16;
+            unsigned char* dst = bank + k * 16;
+            const size_t rstride = (size_t)sw * ES;
+#pragma unroll 2
+            for (int w = tid / cpr; w < W; w += ngroups) {
+                const uint4 x = *reinterpret_cast<const uint4*>(src + w * rstride);
+                const uint64_t d = G == 1 ? d_sh : dw2[w], kv = kv2[w];
+                uint4 y;
+                y.x = P::narrow(ffma2(kv, dp[0], fmul2(P::widen(x.x), d)));
+                y.y = P::narrow(ffma2(kv, dp[1], fmul2(P::widen(x.y), d)));
+                y.z = P::narrow(ffma2(kv, dp[2], fmul2(P::widen(x.z), d)));
+                y.w = P::narrow(ffma2(kv, dp[3], fmul2(P::widen(x.w), d)));
+                *reinterpret_cast<uint4*>(dst + koff[w]) = y;
+            }
+        }
+        if (more) cp_async_wait_all();
+        __syncthreads();
+
+        ldgsts_rows<E>(rows, bank, qoff, R, sw, row_bytes);
+        if (more) {
+            const I* rk = reinterpret_cast<const I*>(smem + L.raw_k);
+            const int lines = (int)((row_bytes + 127) >> 7);
+            const int64_t rowb = (int64_t)hd * ES, colb = (int64_t)c0 * ES;
+            for (int i = tid; i < W * lines; i += nt) {
+                const int r = i / lines, l = i - r * lines;
+                const unsigned char* p = bank + (int64_t)rk[r] * rowb + colb + (int64_t)l * 128;
+                asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+            }
+        }
+        cp_async_wait_all();
+        __syncthreads();
+        if (active) {
+            float acc = 0.0f;
+            int r = 0;
+            for (; r + 4 <= R; r += 4) {
+                const uint4 q = *reinterpret_cast<const uint4*>(qv2 + r);
+                const uint4 q2 = *reinterpret_cast<const uint4*>(qv2 + r + 2);
+                acc = fma_bf16(acc, q.x, rc[(r + 0) * sw]);
+                acc = fma_bf16(acc, q.z, rc[(r + 1) * sw]);
+                acc = fma_bf16(acc, q2.x, rc[(r + 2) * sw]);
+                acc = fma_bf16(acc, q2.z, rc[(r + 3) * sw]);
+            }
+            for (; r < R; ++r) acc = fma_bf16(acc, (uint32_t)qv2[r], rc[r * sw]);
+            out[ts * hd + c0 + j] = from_f32<E>(acc);
+        }
+
+        cp_async_wait_all();
+        __syncthreads();
+        if (t + 1 < a.T) derive_meta<E, I>(a, c0, L, smem);
+        __syncthreads();
+    }
+}
+
 // ---------------------------------------------------------------- streaming path (wide rows)
 // When W or R rows do not fit the shared-memory budget at a useful slice width (e.g. 256 rows of
 // 1 KiB), the rows stream through a ring of NS chunk buffers of CH rows each instead of being
@@ -853,9 +1017,17 @@ auto stream1_kernel() {
     return decode_stream1_kernel<I, NS>;
 }
 
+template <typename I, bool PIECE>
+auto vec1_kernel() {
+    return decode_vec1_kernel<I, PIECE>;
+}
+
 template <typename E, typename I>
 int launch_typed(int path, bool scalar, const DecodeArgs& a, dim3 grid, dim3 block, size_t smem, cudaStream_t stream) {
-    const auto kernel = path == kStaged   ? (a.piece_write ? decode_vec_kernel<E, I, true> : decode_vec_kernel<E, I, false>)
+    const auto kernel = path == kStaged
+                            ? ((sizeof(E) == 2 && scalar)
+                                   ? (a.piece_write ? vec1_kernel<I, true>() : vec1_kernel<I, false>())
+                                   : (a.piece_write ? decode_vec_kernel<E, I, true> : decode_vec_kernel<E, I, false>))
                         : path == kStream
                             ? ((sizeof(E) == 4 && scalar)  // a column per thread
                                    ? (a.stream_stages == 3 ? stream1_kernel<I, 3>() : stream1_kernel<I, 4>())
@@ -956,9 +1128,12 @@ int launch_decode(const DecodeArgs& a0, int bank_dtype, int idx_dtype, cudaStrea
     }
     const int64_t blocks_final = a.n_streams * a.n_slices;
     const int path = !vec ? kSimt : streamed ? kStream : kStaged;
-    // float32 streaming over slices of up to 128 columns: one column per thread (scalar chains,
-    // twice the warps); wider slices keep column pairs (blocks of 256 threads measured slower)
-    const bool scalar = path == kStream && es == 4 && sw <= 128;
+    // One column per thread (scalar chains, twice the warps): float32 streaming over slices of up
+    // to 128 columns (wider slices keep column pairs: blocks of 256 threads measured slower), and
+    // bf16 staged slices of up to 64 columns, the narrow slices of grids with few streams, which
+    // wait on latency and gain from the extra warps (full 256-byte rows of many streams keep
+    // column pairs: 7 % faster there).
+    const bool scalar = (path == kStream && es == 4 && sw <= 128) || (path == kStaged && es == 2 && sw <= 64);
     const int tcols = scalar ? 1 : cpt;
     const int threads = ((sw + tcols - 1) / tcols + 31) / 32 * 32;
     const size_t smem = path == kStaged   ? VecLayout(a.W, a.R, a.G, sw, es, is).total

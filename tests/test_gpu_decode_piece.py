@@ -25,6 +25,7 @@ CASES = [
     ("f32", "i32", 64, 20, 33, 1, 700, 48, 2),
     ("bf16", "i32", 256, 8, 8, 1, 620, 16, 2),
     ("f32", "i64", 32, 5, 5, 5, 700, 8, 4),
+    ("bf16", "i64", 64, 16, 16, 16, 700, 32, 2),   # 128-byte rows: the one-column-per-thread instance
 ]
 
 
