@@ -281,7 +281,8 @@ def test_gather_after_decode_sees_its_writes():
 def test_streamed_decode_many_streams_matches_oracle():
     """Wide rows across many streams: 512 streams of 1 KiB float32 rows with W = R = 256 fill more
     than one wave of blocks, so the streaming path runs 16-row chunks in a four-stage ring (smaller
-    grids take three stages); compared with the oracle on every stream."""
+    grids take three stages), on the one-column-per-thread float32 kernel; compared with the oracle
+    on every stream."""
     wl = workloads.DecodeWorkload("wide_many", "f32", 512, 256, 300, 256, 256, 1, 2, "i64", 1 / 16, bank_std=0.5,
                                   seed=9)
     x = workloads.make_decode_inputs(wl, device=DEV)
@@ -318,3 +319,19 @@ def test_concurrent_calls_on_two_streams_match_sequential():
     assert bits_equal(to_np(out), to_np(ref_out)) and bits_equal(to_np(xd["bank"]), to_np(ref_bank))
     assert all(bits_equal(to_np(a), to_np(b)) for a, b in zip(outs, ref_g))
     assert bits_equal(to_np(stash), to_np(ref_stash))
+
+
+def test_streamed_bf16_four_stage_ring_matches_oracle():
+    """bf16 wide rows in a large grid: 400 streams of 1 KiB rows with W = R = 256 stream through
+    half-row slices (800 blocks) with 16-row chunks in a four-stage ring, on the column-pair
+    streaming kernel; compared with the oracle on every stream."""
+    wl = workloads.DecodeWorkload("wide_bf16_many", "bf16", 400, 512, 300, 256, 256, 1, 2, "i32", 1 / 16,
+                                  bank_std=0.5, seed=17)
+    x = workloads.make_decode_inputs(wl, device=DEV)
+    bank_ref = to_np(x["bank"])
+    ref = oracle.decode_seq(bank_ref, *(to_np(x[k]) for k in DECODE_KEYS))
+    out = sdm.decode_seq(x["bank"], *(x[k] for k in DECODE_KEYS))
+    torch.cuda.synchronize()
+    assert_close(to_np(out), ref, "bf16", "readings")
+    assert_close(to_np(x["bank"]), bank_ref, "bf16", "bank")
+    assert sdm.device_status() == 0
