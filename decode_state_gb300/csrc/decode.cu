@@ -81,6 +81,96 @@ __device__ __forceinline__ uint64_t fmul2(uint64_t a, uint64_t b) {
     return d;
 }
 
+// ---------------------------------------------------------------- gates
+//
+// d = the float32 nearest to e^g, without the double-precision exponential in the common case.
+// Tang's table method (P. T. P. Tang, "Table-driven implementation of the exponential function in
+// IEEE floating-point arithmetic", ACM TOMS 15(2), 1989) in float32 pairs: g = (64m + j) ln2/64 + r
+// with |r| <= 0.00543, and e^g = 2^m 2^(j/64) e^r, where e^r - 1 = r + r^2/2 + r^3 (1/6 + r/24 +
+// r^2/120) truncates below 2^-54. The reduction is exact up to 2^-51 (ln2/64 = A + B + C with A of
+// 9 bits, so nA is exact and g - nA exact; nB an exact product pair), the sum keeps r and r^2/2 as
+// pairs, and the whole evaluation stays within 2^-42 of e^g. The pair is rounded once; the result
+// is taken when the pair lies more than 2^-38 (in units of the scaled value, in [0.99, 2)) inside
+// the rounding interval (Ziv's test, A. Ziv, ACM TOMS 17(3), 1991), and is then the float32 nearest
+// to e^g -- the value that rounding the double-precision exponential gives, which is within 2^-51 of
+// e^g. Otherwise (about one gate in 10^4) and outside [-87, 88] (subnormal, huge or NaN results)
+// the double-precision exponential decides, so every gate has the bits of gate(g).
+
+// 2^(j/64) = hi + lo (each the float32 nearest; the pair within 2^-49 of the power)
+__device__ const float2 kExp2Tab[64] = {
+    {0x1.0p0f, 0.0f}, {0x1.02c9a4p0f, -0x1.887fap-28f},
+    {0x1.059b0ep0f, -0x1.9d4f52p-25f}, {0x1.087452p0f, -0x1.e2990ep-26f},
+    {0x1.0b5586p0f, 0x1.9f3122p-25f}, {0x1.0e3ec4p0f, -0x1.a585ccp-25f},
+    {0x1.11301ep0f, -0x1.fdb496p-25f}, {0x1.1429aap0f, 0x1.d525bcp-25f},
+    {0x1.172b84p0f, -0x1.c15742p-27f}, {0x1.1a35bep0f, 0x1.6df96ep-25f},
+    {0x1.1d4874p0f, -0x1.d2e8cap-25f}, {0x1.2063b8p0f, 0x1.0c519ap-25f},
+    {0x1.2387a6p0f, 0x1.ceac48p-25f}, {0x1.26b456p0f, 0x1.789f38p-26f},
+    {0x1.29e9ep0f, -0x1.5c0424p-25f}, {0x1.2d285ap0f, 0x1.b900c2p-26f},
+    {0x1.306fep0f, 0x1.4636e2p-25f}, {0x1.33c08cp0f, -0x1.b37d2p-25f},
+    {0x1.371a74p0f, -0x1.18aac6p-25f}, {0x1.3a7db4p0f, -0x1.634c02p-25f},
+    {0x1.3dea64p0f, 0x1.824684p-25f}, {0x1.4160a2p0f, 0x1.f72e2ap-28f},
+    {0x1.44e086p0f, 0x1.8624b4p-30f}, {0x1.486a2cp0f, -0x1.47d866p-25f},
+    {0x1.4bfdaep0f, -0x1.593abcp-25f}, {0x1.4f9b28p0f, -0x1.2c5a6cp-25f},
+    {0x1.5342b6p0f, -0x1.2c561p-25f}, {0x1.56f474p0f, -0x1.295b04p-25f},
+    {0x1.5ab07ep0f, -0x1.5bd5ecp-27f}, {0x1.5e76f2p0f, -0x1.4a5bd6p-25f},
+    {0x1.6247ecp0f, -0x1.f8b55p-25f}, {0x1.662388p0f, 0x1.2a9112p-27f},
+    {0x1.6a09e6p0f, 0x1.9fcef4p-26f}, {0x1.6dfb24p0f, -0x1.cd72e8p-27f},
+    {0x1.71f75ep0f, 0x1.1d8beep-25f}, {0x1.75feb6p0f, -0x1.37b306p-25f},
+    {0x1.7a1148p0f, -0x1.829fdp-25f}, {0x1.7e2f34p0f, -0x1.261634p-25f},
+    {0x1.82589ap0f, -0x1.accc7cp-26f}, {0x1.868d9ap0f, -0x1.2edb44p-26f},
+    {0x1.8ace54p0f, 0x1.15506ep-27f}, {0x1.8f1aeap0f, -0x1.baa232p-26f},
+    {0x1.93737cp0f, -0x1.e64744p-25f}, {0x1.97d82ap0f, -0x1.0d8d84p-31f},
+    {0x1.9c4918p0f, 0x1.51f848p-27f}, {0x1.a0c668p0f, -0x1.2886a6p-26f},
+    {0x1.a5503cp0f, -0x1.b83b54p-25f}, {0x1.a9e6b6p0f, -0x1.50c048p-25f},
+    {0x1.ae89fap0f, -0x1.a94b14p-26f}, {0x1.b33a2cp0f, -0x1.ec3a82p-26f},
+    {0x1.b7f77p0f, -0x1.a09438p-25f}, {0x1.bcc1eap0f, -0x1.f687c6p-25f},
+    {0x1.c199bep0f, -0x1.3d56b2p-27f}, {0x1.c67f12p0f, 0x1.cafa2ap-25f},
+    {0x1.cb720ep0f, -0x1.8837ccp-27f}, {0x1.d072d4p0f, 0x1.40f13p-25f},
+    {0x1.d5818ep0f, -0x1.822dbcp-27f}, {0x1.da9e6p0f, 0x1.ed9942p-27f},
+    {0x1.dfc974p0f, -0x1.908c94p-25f}, {0x1.e502eep0f, 0x1.e2cffep-26f},
+    {0x1.ea4afap0f, 0x1.52486cp-27f}, {0x1.efa1bep0f, 0x1.cc2b44p-25f},
+    {0x1.f50766p0f, -0x1.246ebp-26f}, {0x1.fa7c18p0f, 0x1.9e90d8p-28f},
+};
+
+// the error of s = a + b (rounded): a + b = s + two_sum_err(a, b, s) exactly
+__device__ __forceinline__ float two_sum_err(float a, float b, float s) {
+    const float bb = __fsub_rn(s, a);
+    return __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
+}
+
+__device__ __forceinline__ float gate(float g) {
+    if (fabsf(g) < 0x1p-30f) return 1.0f;  // e^g within 2^-30 of 1, far from both rounding midpoints
+    if (!(g >= -87.0f && g <= 88.0f)) return (float)exp((double)g);
+    constexpr float kInv = 0x1.715476p6f;  // 64 / ln2
+    constexpr float kA = 0x1.63p-7f, kB = -0x1.bd0106p-19f, kC = 0x1.cf79acp-46f;  // ln2/64 = A + B + C
+    const float nf = rintf(__fmul_rn(g, kInv));  // |n| <= 8126
+    const int n = (int)nf, j = n & 63, m = n >> 6;  // n = 64m + j, 0 <= j < 64
+    const float t1 = fmaf(-nf, kA, g);               // g - nA, exact
+    const float p_hi = __fmul_rn(nf, kB);
+    const float p_lo = fmaf(nf, kB, -p_hi);          // nB = p_hi + p_lo exactly
+    const float r_hi = __fsub_rn(t1, p_hi);
+    const float r_lo = __fsub_rn(__fsub_rn(two_sum_err(t1, -p_hi, r_hi), p_lo), __fmul_rn(nf, kC));
+    const float s_hi = __fmul_rn(r_hi, r_hi);
+    const float s_lo = fmaf(r_hi, r_hi, -s_hi);      // r_hi^2 = s_hi + s_lo exactly
+    const float h = __fmul_rn(0.5f, s_hi);
+    const float u_hi = __fadd_rn(r_hi, h);
+    const float cubic = __fmul_rn(__fmul_rn(r_hi, s_hi),
+                                  fmaf(r_hi, fmaf(r_hi, 1.0f / 120.0f, 1.0f / 24.0f), 1.0f / 6.0f));
+    const float low = two_sum_err(r_hi, h, u_hi) + r_lo + (0.5f * s_lo + r_hi * r_lo) + cubic;
+    const float e_hi = __fadd_rn(1.0f, u_hi);        // e^r = e_hi + e_lo
+    const float e_lo = __fadd_rn(__fadd_rn(__fsub_rn(1.0f, e_hi), u_hi), low);
+    const float2 t = __ldg(&kExp2Tab[j]);
+    const float y_hi = __fmul_rn(t.x, e_hi);         // 2^(j/64) e^r = y_hi + y_lo
+    const float y_lo = fmaf(t.y, e_hi, fmaf(t.x, e_lo, fmaf(t.x, e_hi, -y_hi)));
+    const float f = __fadd_rn(y_hi, y_lo);
+    const float dev = __fadd_rn(__fsub_rn(y_hi, f), y_lo);  // (y_hi + y_lo) - f, to 2^-48
+    const uint32_t fb = __float_as_uint(f);
+    const float ulp = __uint_as_float((fb & 0x7f800000u) - (23u << 23));
+    const float half = (dev < 0.0f && (fb & 0x007fffffu) == 0) ? 0.25f * ulp : 0.5f * ulp;
+    if (fabsf(dev) < half - 0x1p-38f) return __uint_as_float(fb + ((uint32_t)m << 23));  // f 2^m, normal
+    return (float)exp((double)g);
+}
+
 // lo += q * x.lo, hi += q * x.hi for a bf16 pair x, with q the bf16 held in the high half of the
 // float32 bit pattern qbits (exact when the float32 is bf16-representable); one rounding each
 __device__ __forceinline__ void fma_bf16_pair(float& lo, float& hi, uint32_t qbits, uint32_t x) {
@@ -200,7 +290,7 @@ __device__ __forceinline__ void derive_meta(const DecodeArgs& a, int c0, const V
     for (int i = tid; i < W; i += nt) {
         koff[i] = (int64_t)rk[i] * rowb + colb;
         const float k = round_to<E>(rkv[i]);
-        const float d = G == 1 ? d1 : (float)exp((double)rg[i]);
+        const float d = G == 1 ? d1 : gate(rg[i]);
         const float aa = __fmul_rn(k, d);
         kv2[i] = f2(k, k);
         aw2[i] = f2(aa, aa);
@@ -281,7 +371,7 @@ __global__ void __launch_bounds__(kMaxThreads, 2) decode_vec_kernel(const Decode
     cp_async_wait_all();
     __syncthreads();
     if (G == 1 && tid == 0)
-        *reinterpret_cast<float*>(smem + L.dnext) = (float)exp((double)*reinterpret_cast<const float*>(smem + L.raw_g));
+        *reinterpret_cast<float*>(smem + L.dnext) = gate(*reinterpret_cast<const float*>(smem + L.raw_g));
     __syncthreads();
     derive_meta<E, I>(a, c0, L, smem);
     __syncthreads();
@@ -309,7 +399,7 @@ __global__ void __launch_bounds__(kMaxThreads, 2) decode_vec_kernel(const Decode
         if (more) {
             prefetch_meta<I>(a, ts + a.n_streams, L, smem);
             if (G == 1 && tid == 0)  // the next token's shared gate, while this token's rows are in flight
-                *reinterpret_cast<float*>(smem + L.dnext) = (float)exp((double)__ldg(a.g + ts + a.n_streams));
+                *reinterpret_cast<float*>(smem + L.dnext) = gate(__ldg(a.g + ts + a.n_streams));
         }
         if (more)
             asm volatile("cp.async.wait_group 1;" ::: "memory");  // the rows, not yet the metadata
@@ -503,7 +593,7 @@ __global__ void __launch_bounds__(128, 7) decode_vec1_kernel(const DecodeArgs a,
     cp_async_wait_all();
     __syncthreads();
     if (G == 1 && tid == 0)
-        *reinterpret_cast<float*>(smem + L.dnext) = (float)exp((double)*reinterpret_cast<const float*>(smem + L.raw_g));
+        *reinterpret_cast<float*>(smem + L.dnext) = gate(*reinterpret_cast<const float*>(smem + L.raw_g));
     __syncthreads();
     derive_meta<E, I>(a, c0, L, smem);
     __syncthreads();
@@ -526,7 +616,7 @@ __global__ void __launch_bounds__(128, 7) decode_vec1_kernel(const DecodeArgs a,
         if (more) {
             prefetch_meta<I>(a, ts + a.n_streams, L, smem);
             if (G == 1 && tid == 0)
-                *reinterpret_cast<float*>(smem + L.dnext) = (float)exp((double)__ldg(a.g + ts + a.n_streams));
+                *reinterpret_cast<float*>(smem + L.dnext) = gate(__ldg(a.g + ts + a.n_streams));
         }
         if (more)
             asm volatile("cp.async.wait_group 1;" ::: "memory");
@@ -693,7 +783,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) decode_stream_kernel(const Dec
     cp_async_wait_all();
     __syncthreads();
     if (G == 1 && tid == 0)
-        *reinterpret_cast<float*>(smem + L.dnext) = (float)exp((double)*reinterpret_cast<const float*>(smem + L.raw_g));
+        *reinterpret_cast<float*>(smem + L.dnext) = gate(*reinterpret_cast<const float*>(smem + L.raw_g));
     __syncthreads();
     derive_meta<E, I>(a, c0, L, smem);
     __syncthreads();
@@ -756,7 +846,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) decode_stream_kernel(const Dec
         if (more) {
             prefetch_meta<I>(a, ts + a.n_streams, L, smem);
             if (G == 1 && tid == 0)
-                *reinterpret_cast<float*>(smem + L.dnext) = (float)exp((double)__ldg(a.g + ts + a.n_streams));
+                *reinterpret_cast<float*>(smem + L.dnext) = gate(__ldg(a.g + ts + a.n_streams));
         }
         uint64_t racc = 0;
         for (int q = 0; q < NS - 1; ++q) {
@@ -831,7 +921,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) decode_stream1_kernel(const De
     cp_async_wait_all();
     __syncthreads();
     if (G == 1 && tid == 0)
-        *reinterpret_cast<float*>(smem + L.dnext) = (float)exp((double)*reinterpret_cast<const float*>(smem + L.raw_g));
+        *reinterpret_cast<float*>(smem + L.dnext) = gate(*reinterpret_cast<const float*>(smem + L.raw_g));
     __syncthreads();
     derive_meta<float, I>(a, c0, L, smem);
     __syncthreads();
@@ -882,7 +972,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) decode_stream1_kernel(const De
         if (more) {
             prefetch_meta<I>(a, ts + a.n_streams, L, smem);
             if (G == 1 && tid == 0)
-                *reinterpret_cast<float*>(smem + L.dnext) = (float)exp((double)__ldg(a.g + ts + a.n_streams));
+                *reinterpret_cast<float*>(smem + L.dnext) = gate(__ldg(a.g + ts + a.n_streams));
         }
         float racc = 0.0f;
         for (int q = 0; q < NS - 1; ++q) {
@@ -977,9 +1067,9 @@ __global__ void __launch_bounds__(kMaxThreads) decode_simt_kernel(const DecodeAr
             const int64_t e = ts * W + i;
             k_slot[i] = load_index<I>(a.k_idx, e);
             kv[i] = round_to<E>(__ldg(a.k_val + e));
-            if (G != 1) dw[i] = (float)exp((double)__ldg(a.g + ts * G + i));
+            if (G != 1) dw[i] = gate(__ldg(a.g + ts * G + i));
         }
-        if (G == 1 && tid == 0) dw[0] = (float)exp((double)__ldg(a.g + ts));
+        if (G == 1 && tid == 0) dw[0] = gate(__ldg(a.g + ts));
         for (int i = tid; i < R; i += nt) {
             const int64_t e = ts * R + i;
             q_slot[i] = load_index<I>(a.q_idx, e);
