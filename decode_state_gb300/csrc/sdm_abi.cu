@@ -93,13 +93,9 @@ int check_decode(void* bank, const void* k_idx, const float* k_val, const float*
     return SDM_OK;
 }
 
-}  // namespace
-
-extern "C" {
-
-int sdm_decode_seq(void* bank, const void* k_idx, const float* k_val, const float* v, const float* beta,
-                   const float* g, const void* q_idx, const float* q_val, void* out, int64_t n_streams, int hd,
-                   int W, int R, int G, int T, int bank_dtype, int idx_dtype, sdm_stream_t stream) {
+int decode_common(void* bank, const void* k_idx, const float* k_val, const float* v, const float* beta,
+                  const float* g, const void* q_idx, const float* q_val, void* out, int64_t n_streams, int hd, int W,
+                  int R, int G, int T, int bank_dtype, int idx_dtype, int inputs_ready, sdm_stream_t stream) {
     const int rc = check_decode(bank, k_idx, k_val, v, beta, g, q_idx, q_val, out, n_streams, hd, W, R, G, T,
                                 bank_dtype, idx_dtype);
     if (rc != SDM_OK || n_streams == 0 || T == 0) return rc;
@@ -119,14 +115,34 @@ int sdm_decode_seq(void* bank, const void* k_idx, const float* k_val, const floa
     a.R = R;
     a.G = G;
     a.T = T;
+    a.inputs_ready = inputs_ready;
     return sdm::launch_decode(a, bank_dtype, idx_dtype, reinterpret_cast<cudaStream_t>(stream));
+}
+
+}  // namespace
+
+extern "C" {
+
+int sdm_decode_seq(void* bank, const void* k_idx, const float* k_val, const float* v, const float* beta,
+                   const float* g, const void* q_idx, const float* q_val, void* out, int64_t n_streams, int hd,
+                   int W, int R, int G, int T, int bank_dtype, int idx_dtype, sdm_stream_t stream) {
+    return decode_common(bank, k_idx, k_val, v, beta, g, q_idx, q_val, out, n_streams, hd, W, R, G, T, bank_dtype,
+                         idx_dtype, 0, stream);
 }
 
 int sdm_decode_step(void* bank, const void* k_idx, const float* k_val, const float* v, const float* beta,
                     const float* g, const void* q_idx, const float* q_val, void* out, int64_t n_streams, int hd,
                     int W, int R, int G, int bank_dtype, int idx_dtype, sdm_stream_t stream) {
-    return sdm_decode_seq(bank, k_idx, k_val, v, beta, g, q_idx, q_val, out, n_streams, hd, W, R, G, 1, bank_dtype,
-                          idx_dtype, stream);
+    return decode_common(bank, k_idx, k_val, v, beta, g, q_idx, q_val, out, n_streams, hd, W, R, G, 1, bank_dtype,
+                         idx_dtype, 0, stream);
+}
+
+int sdm_decode_step_ex(void* bank, const void* k_idx, const float* k_val, const float* v, const float* beta,
+                       const float* g, const void* q_idx, const float* q_val, void* out, int64_t n_streams, int hd,
+                       int W, int R, int G, int bank_dtype, int idx_dtype, unsigned flags, sdm_stream_t stream) {
+    if (flags & ~SDM_INPUTS_READY) return SDM_EFLAGS;
+    return decode_common(bank, k_idx, k_val, v, beta, g, q_idx, q_val, out, n_streams, hd, W, R, G, 1, bank_dtype,
+                         idx_dtype, (flags & SDM_INPUTS_READY) ? 1 : 0, stream);
 }
 
 }  // extern "C"
@@ -312,6 +328,7 @@ const char* sdm_status_string(int status) {
         case SDM_EPLAN: return "not a gather plan made by sdm_gather_plan_init in this process";
         case SDM_EROW: return "row0 outside 0..row0_max, or row0_max + tokens beyond the index rows";
         case SDM_EDEVICE: return "the current device is not the gather plan's device";
+        case SDM_EFLAGS: return "unknown bits in the flags of sdm_decode_step_ex";
         default: break;
     }
     if (status > 0) return cudaGetErrorString(static_cast<cudaError_t>(status));
@@ -328,6 +345,6 @@ int sdm_device_status(unsigned int* status, int clear) {
     return e;
 }
 
-int sdm_version(void) { return 100; }
+int sdm_version(void) { return 200; }
 
 }  // extern "C"

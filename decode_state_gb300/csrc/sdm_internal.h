@@ -24,6 +24,7 @@ struct DecodeArgs {
     int stream_rows;    // rows per ring chunk of the streaming path
     int stream_stages;  // chunk buffers in its ring (3 or 4)
     int piece_write;  // staged path: decay-and-write by 16-byte pieces (many blocks per SM)
+    int inputs_ready; // the inputs predate the preceding kernel: load them before waiting on it
 };
 
 struct GatherArgs {

@@ -5,7 +5,9 @@ them can be captured once and replayed. ``DecodeStepGraph`` captures T single-to
 ``sdm_decode_step`` launches (one per token, each reading its own slab of fixed device input
 buffers) into one graph: fill ``inputs`` (device tensors, time-major [T, S, .]) and call
 ``replay()``; the readings land in ``out`` [T, S, hd]. This replaces T separate host calls (and
-their per-call argument checks) by one graph launch; the kernels are the same.
+their per-call argument checks) by one graph launch; the kernels are the same. Since every input
+is in place before the replay starts, each step is launched with SDM_INPUTS_READY: it loads its
+metadata and warms L2 with its rows while the step before it still runs.
 """
 
 from __future__ import annotations
@@ -42,7 +44,8 @@ class DecodeStepGraph:
 
     def _steps(self):
         for t in range(self.T):
-            sdm.decode_step(self.bank, *(self.inputs[k][t] for k in DECODE_INPUTS), out=self.out[t])
+            sdm.decode_step(self.bank, *(self.inputs[k][t] for k in DECODE_INPUTS), out=self.out[t],
+                            inputs_ready=True)
 
     def replay(self) -> torch.Tensor:
         """Run the T captured steps on the current contents of ``inputs``; returns ``out``."""

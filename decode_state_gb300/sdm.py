@@ -20,8 +20,10 @@ SDM_BF16, SDM_F32 = 0, 1
 SDM_I32, SDM_I64 = 0, 1
 SDM_DEV_TIMEOUT, SDM_DEV_BAD_INDEX = 1, 2
 
-ENTRY_POINTS = ("sdm_decode_step", "sdm_decode_seq", "sdm_gather", "sdm_gather_kpos", "sdm_gather_plan_init",
-                "sdm_gather_plan_launch", "sdm_status_string", "sdm_device_status", "sdm_version")
+ENTRY_POINTS = ("sdm_decode_step", "sdm_decode_step_ex", "sdm_decode_seq", "sdm_gather", "sdm_gather_kpos",
+                "sdm_gather_plan_init", "sdm_gather_plan_launch", "sdm_status_string", "sdm_device_status",
+                "sdm_version")
+SDM_INPUTS_READY = 1  # sdm_decode_step_ex flag: the inputs predate the kernel launched just before
 GATHER_PLAN_BYTES = 512  # SDM_GATHER_PLAN_BYTES
 
 _BANK_CODES = {torch.bfloat16: SDM_BF16, torch.float32: SDM_F32}
@@ -54,6 +56,8 @@ def library() -> ctypes.CDLL:
             dec = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i64, i32, i32, i32, i32]
             lib.sdm_decode_step.argtypes = dec + [i32, i32, vp]
             lib.sdm_decode_step.restype = i32
+            lib.sdm_decode_step_ex.argtypes = dec + [i32, i32, ctypes.c_uint, vp]
+            lib.sdm_decode_step_ex.restype = i32
             lib.sdm_decode_seq.argtypes = dec + [i32, i32, i32, vp]
             lib.sdm_decode_seq.restype = i32
             lib.sdm_gather.argtypes = [vp, i64, i32, i32, i32, ctypes.POINTER(vp), ctypes.POINTER(vp),
@@ -140,13 +144,23 @@ def _decode_args(bank, k_idx, k_val, v, beta, g, q_idx, q_val, out, lead: tuple,
                  q_idx.data_ptr(), q_val.data_ptr(), out.data_ptr()), hd, W, R, G, _stream_handle(stream, dev)
 
 
-def decode_step(bank, k_idx, k_val, v, beta, g, q_idx, q_val, out=None, stream=None) -> torch.Tensor:
+def decode_step(bank, k_idx, k_val, v, beta, g, q_idx, q_val, out=None, stream=None,
+                inputs_ready: bool = False) -> torch.Tensor:
     """One write-then-read token for every stream (sdm_decode_step). Per-stream arrays are [S, .],
-    beta is [S]; the bank is updated in place; returns the readings [S, hd] in the bank dtype."""
+    beta is [S]; the bank is updated in place; returns the readings [S, hd] in the bank dtype.
+
+    ``inputs_ready`` (sdm_decode_step_ex with SDM_INPUTS_READY) promises that the inputs were
+    complete before the kernel enqueued just ahead of this call began; the launch then loads them
+    and warms L2 with the step's rows while that kernel still runs. Same results."""
     S = k_idx.shape[0]
     out, ptrs, hd, W, R, G, st = _decode_args(bank, k_idx, k_val, v, beta, g, q_idx, q_val, out, (S,), stream)
-    rc = library().sdm_decode_step(*ptrs, S, hd, W, R, G, _BANK_CODES[bank.dtype], _IDX_CODES[k_idx.dtype], st)
-    _check("sdm_decode_step", rc)
+    codes = (_BANK_CODES[bank.dtype], _IDX_CODES[k_idx.dtype])
+    if inputs_ready:
+        rc = library().sdm_decode_step_ex(*ptrs, S, hd, W, R, G, *codes, SDM_INPUTS_READY, st)
+        _check("sdm_decode_step_ex", rc)
+    else:
+        rc = library().sdm_decode_step(*ptrs, S, hd, W, R, G, *codes, st)
+        _check("sdm_decode_step", rc)
     return out
 
 
@@ -254,11 +268,14 @@ class DecodeStepPlan:
     the readings into ``out[t]`` ([T, S, hd], allocated when not given). Shapes, dtypes, devices
     and every step's pointers are settled here, so a launch is one foreign call. The plan keeps
     references to its tensors; they must not be resized or reallocated in place.
+
+    With ``inputs_ready`` every launch passes SDM_INPUTS_READY (sdm_decode_step_ex): the caller
+    fills all T slabs before the launches, not between them.
     """
 
     DECODE_KEYS = ("k_idx", "k_val", "v", "beta", "g", "q_idx", "q_val")
 
-    def __init__(self, bank, inputs: dict, out=None, stream=None):
+    def __init__(self, bank, inputs: dict, out=None, stream=None, inputs_ready: bool = False):
         T = inputs["k_idx"].shape[0]
         if out is None:
             out = torch.empty((T, inputs["k_idx"].shape[1], bank.shape[1]), dtype=bank.dtype, device=bank.device)
@@ -266,8 +283,11 @@ class DecodeStepPlan:
         self.out, _, hd, W, R, G, _ = _decode_args(bank, *args, out, (T, inputs["k_idx"].shape[1]), stream)
         S = inputs["k_idx"].shape[1]
         self._tail = (S, hd, W, R, G, _BANK_CODES[bank.dtype], _IDX_CODES[inputs["k_idx"].dtype])
+        if inputs_ready:
+            self._tail += (SDM_INPUTS_READY,)
         self._steps = [(bank.data_ptr(), *(a[t].data_ptr() for a in args), self.out[t].data_ptr()) for t in range(T)]
-        self._fn = library().sdm_decode_step
+        self._name = "sdm_decode_step_ex" if inputs_ready else "sdm_decode_step"
+        self._fn = getattr(library(), self._name)
         self._stream = _stream_handle(stream, bank.device) if stream is not None else None
         self._keep = (bank, inputs)
         self.device, self.T = bank.device, T
@@ -277,7 +297,7 @@ class DecodeStepPlan:
         st = self._stream if stream is None and self._stream is not None else _stream_handle(stream, self.device)
         rc = self._fn(*self._steps[t], *self._tail, st)
         if rc != 0:
-            _check("sdm_decode_step", rc)
+            _check(self._name, rc)
         return self.out[t]
 
 

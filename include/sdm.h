@@ -66,6 +66,7 @@ typedef struct CUstream_st* sdm_stream_t;
 #define SDM_EPLAN (-12)     /* not an initialised gather plan (wrong tag or record size) */
 #define SDM_EROW (-13)      /* row0 outside 0..row0_max, or row0_max + tokens beyond the index rows */
 #define SDM_EDEVICE (-14)   /* the current device is not the one the gather plan was made on */
+#define SDM_EFLAGS (-15)    /* unknown bits in the flags of sdm_decode_step_ex */
 
 /* bits of the device status word */
 #define SDM_DEV_TIMEOUT 1u   /* reserved: a kernel gave up a bounded wait (no current kernel waits) */
@@ -98,6 +99,23 @@ typedef struct CUstream_st* sdm_stream_t;
 int sdm_decode_step(void* bank, const void* k_idx, const float* k_val, const float* v, const float* beta,
                     const float* g, const void* q_idx, const float* q_val, void* out, int64_t n_streams, int hd,
                     int W, int R, int G, int bank_dtype, int idx_dtype, sdm_stream_t stream);
+
+/*
+ * sdm_decode_step_ex - sdm_decode_step with flags; flags == 0 is sdm_decode_step.
+ *
+ * SDM_INPUTS_READY promises that every input but the bank (k_idx, k_val, v, beta, g, q_idx,
+ * q_val) was complete before the kernel enqueued just ahead of this launch on the stream began.
+ * The launch may then read them, derive the token's weights and gates and warm L2 with the
+ * token's bank rows before it waits for that kernel (the launches of this library chain by
+ * programmatic dependent launch); it reads and writes the bank, and writes `out`, only after the
+ * wait. Results are the same bits as without the flag. Use it for steps whose inputs are staged
+ * ahead (e.g. one CUDA graph of many steps over inputs filled before the replay); without the
+ * promise the flag may read stale inputs. Unknown bits return SDM_EFLAGS.
+ */
+#define SDM_INPUTS_READY 1u
+int sdm_decode_step_ex(void* bank, const void* k_idx, const float* k_val, const float* v, const float* beta,
+                       const float* g, const void* q_idx, const float* q_val, void* out, int64_t n_streams, int hd,
+                       int W, int R, int G, int bank_dtype, int idx_dtype, unsigned flags, sdm_stream_t stream);
 
 /*
  * sdm_decode_seq - T tokens for every stream in one launch, equal to T sdm_decode_step calls.

@@ -40,7 +40,7 @@ def test_header_declares_the_entry_points():
 def test_library_exports_every_declared_symbol(lib):
     for name in sdm.ENTRY_POINTS:
         assert hasattr(lib, name), name
-    assert sdm.version() == 100
+    assert sdm.version() == 200
 
 
 def test_status_strings(lib):
@@ -73,6 +73,16 @@ def _decode(lib, **kw):
 ])
 def test_decode_argument_errors(lib, kw, code):
     assert _decode(lib, **kw) == CODES[code]
+
+
+def test_decode_step_ex_flags(lib):
+    """Unknown flag bits are refused before anything else; the known flag validates like the step."""
+    args = (FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4, 64, 8, 8, 1, 0, 0)
+    assert lib.sdm_decode_step_ex(*args, 2, None) == CODES["SDM_EFLAGS"]
+    assert lib.sdm_decode_step_ex(*args, 0x80000000, None) == CODES["SDM_EFLAGS"]
+    bad = (FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4, 64, 0, 8, 1, 0, 0)
+    assert lib.sdm_decode_step_ex(*bad, sdm.SDM_INPUTS_READY, None) == CODES["SDM_EWIDTH"]
+    assert lib.sdm_decode_step_ex(*args[:9], 0, *args[10:], sdm.SDM_INPUTS_READY, None) == 0  # no streams
 
 
 def test_decode_step_validates_like_seq(lib):
