@@ -519,8 +519,27 @@ def extras(args, dev, r: sdist.Rank, peak: float, skip: str):
             item.update({"graph_unit_per_s": case.units / (gms / 1e3), "graph_ms_per_step": gms,
                          "graph_us_per_launch": gms * 1e3 / case.launches})
             del graph
-            # the same launches eagerly through a plan (checked once, pointers precomputed)
             from decode_state_gb300 import sdm
+
+            # the graph again with every launch promising its inputs staged ahead (SDM_INPUTS_READY,
+            # as DecodeStepGraph does): the inputs are written before the replay starts
+            def ready_steps():
+                for t in range(case.wl.T):
+                    sdm.decode_step(case.x["bank"], *(case.x[k][t] for k in DECODE_KEYS), out=case.out[t],
+                                    inputs_ready=True)
+
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.stream(s):
+                ready_steps()
+                torch.cuda.synchronize()
+                with torch.cuda.graph(graph, stream=s):
+                    ready_steps()
+            torch.cuda.current_stream(dev).wait_stream(s)
+            rgms = _time_calls(graph.replay, reps, 1)
+            item.update({"graph_ready_unit_per_s": case.units / (rgms / 1e3), "graph_ready_ms_per_step": rgms,
+                         "graph_ready_us_per_launch": rgms * 1e3 / case.launches})
+            del graph
+            # the same launches eagerly through a plan (checked once, pointers precomputed)
 
             plan = sdm.DecodeStepPlan(case.x["bank"], {k: case.x[k] for k in DECODE_KEYS}, out=case.out,
                                       stream=torch.cuda.current_stream(dev))
@@ -532,6 +551,13 @@ def extras(args, dev, r: sdist.Rank, peak: float, skip: str):
             pms = _time_calls(plan_steps, reps)
             item.update({"plan_unit_per_s": case.units / (pms / 1e3), "plan_ms_per_step": pms,
                          "plan_us_per_launch": pms * 1e3 / case.launches})
+            # the same plan promising inputs staged ahead (SDM_INPUTS_READY): each launch loads its
+            # metadata and warms L2 while the launch ahead of it still runs
+            plan = sdm.DecodeStepPlan(case.x["bank"], {k: case.x[k] for k in DECODE_KEYS}, out=case.out,
+                                      stream=torch.cuda.current_stream(dev), inputs_ready=True)
+            rms = _time_calls(plan_steps, reps)
+            item.update({"plan_ready_unit_per_s": case.units / (rms / 1e3), "plan_ready_ms_per_step": rms,
+                         "plan_ready_us_per_launch": rms * 1e3 / case.launches})
             del plan
         res[name] = item
         del case
