@@ -582,12 +582,16 @@ def plan_slabs(dev, slab: int = 256) -> dict:
         for k in range(n):
             plan.launch(k * slab)
 
+    def via_plan_ready():  # the index rows exist before the walk: SDM_INPUTS_READY holds
+        for k in range(n):
+            plan.launch(k * slab, inputs_ready=True)
+
     def direct():
         for k in range(n):
             sdm.gather(g["bank"], slabs[k], chunk=wl.chunk, outs=outs, with_stash=False)
 
     res = {"slab_tokens": slab, "launches_per_walk": n}
-    for name, fn in (("plan", via_plan), ("direct", direct)):
+    for name, fn in (("plan", via_plan), ("plan_ready", via_plan_ready), ("direct", direct)):
         ms = _time_calls(fn, 5)
         torch.cuda.synchronize()
         t0 = time.perf_counter()
@@ -595,6 +599,18 @@ def plan_slabs(dev, slab: int = 256) -> dict:
         host_us = (time.perf_counter() - t0) * 1e6 / n
         torch.cuda.synchronize()
         res[name] = {"ms_per_walk": ms, "us_per_launch": ms * 1e3 / n, "host_us_per_call": host_us}
+    # the plan walks replayed from CUDA graphs: device time per launch without the host calls
+    side = torch.cuda.Stream(dev)
+    for name, fn in (("plan_graph", via_plan), ("plan_ready_graph", via_plan_ready)):
+        graph = torch.cuda.CUDAGraph()
+        side.wait_stream(torch.cuda.current_stream(dev))
+        with torch.cuda.stream(side):
+            with torch.cuda.graph(graph, stream=side):
+                fn()
+        torch.cuda.current_stream(dev).wait_stream(side)
+        ms = _time_calls(graph.replay, 5, 1)
+        res[name] = {"ms_per_walk": ms, "us_per_launch": ms * 1e3 / n}
+        del graph
     return res
 
 

@@ -97,10 +97,15 @@ __global__ void __launch_bounds__(kMaxThreads) gather_kernel(const GatherArgs a,
     const E* bank = static_cast<const E*>(a.bank);
     E* stash = static_cast<E*>(a.stash);
 
-    grid_dependency_wait();
+    // With inputs_ready the index and weight rows predate the preceding kernel: they are read, and
+    // the rows they name warmed in L2, before waiting for that kernel; the bank is read and the
+    // outputs written only after the wait (L2 is the point of coherence: a line warmed early still
+    // holds every later write to it).
+    if (!a.inputs_ready) grid_dependency_wait();
     if (early_trigger) grid_launch_dependents();
     const int vt = a.chunk_valid != nullptr ? __ldg(a.chunk_valid + t / a.chunk) : a.valid;
     if ((int)(t % a.chunk) >= vt) {
+        if (a.inputs_ready) grid_dependency_wait();
         write_padding<E>(a, t, c0, ncols, j, active, stash_bulk && a.n_slices == 1);
         return;
     }
@@ -128,6 +133,16 @@ __global__ void __launch_bounds__(kMaxThreads) gather_kernel(const GatherArgs a,
     // compact snapshot: this token's chunk block
     E* compact = a.kpos != nullptr ? stash + (t / a.chunk) * ((int64_t)a.chunk * W0) * hd : nullptr;
     __syncthreads();
+    if (a.inputs_ready) {
+        const unsigned char* src = reinterpret_cast<const unsigned char*>(bank) + (int64_t)c0 * ES;
+        const int64_t rowb = (int64_t)hd * ES;
+        const int lines = (int)((row_bytes + 127) >> 7);
+        for (int i = tid; i < NR * lines; i += nt) {
+            const int e = i / lines, l = i - e * lines;
+            if (slot[e] >= 0) asm volatile("prefetch.global.L2 [%0];" ::"l"(src + slot[e] * rowb + (int64_t)l * 128));
+        }
+        grid_dependency_wait();
+    }
 
     if (BULK) {
         // every thread: 16-byte cp.async copies of the entry row slices (zeros for skipped entries)

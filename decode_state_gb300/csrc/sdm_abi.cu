@@ -289,6 +289,12 @@ int sdm_gather_plan_init(sdm_gather_plan* plan, const void* bank, int64_t n_slot
 }
 
 int sdm_gather_plan_launch(const sdm_gather_plan* plan, int64_t row0, int valid, sdm_stream_t stream) {
+    return sdm_gather_plan_launch_ex(plan, row0, valid, 0u, stream);
+}
+
+int sdm_gather_plan_launch_ex(const sdm_gather_plan* plan, int64_t row0, int valid, unsigned flags,
+                              sdm_stream_t stream) {
+    if (flags & ~SDM_INPUTS_READY) return SDM_EFLAGS;
     if (!plan) return SDM_ENULL;
     PlanRecord p;
     std::memcpy(&p, plan, sizeof(p));
@@ -308,6 +314,7 @@ int sdm_gather_plan_launch(const sdm_gather_plan* plan, int64_t row0, int valid,
         a.w[o] = static_cast<const unsigned char*>(a.w[o]) + row0 * p.w_row_bytes[o];
     }
     a.valid = valid;
+    a.inputs_ready = (flags & SDM_INPUTS_READY) ? 1 : 0;
     return sdm::run_gather(p.launch, reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -328,7 +335,7 @@ const char* sdm_status_string(int status) {
         case SDM_EPLAN: return "not a gather plan made by sdm_gather_plan_init in this process";
         case SDM_EROW: return "row0 outside 0..row0_max, or row0_max + tokens beyond the index rows";
         case SDM_EDEVICE: return "the current device is not the gather plan's device";
-        case SDM_EFLAGS: return "unknown bits in the flags of sdm_decode_step_ex";
+        case SDM_EFLAGS: return "unknown bits in the flags of an _ex entry point";
         default: break;
     }
     if (status > 0) return cudaGetErrorString(static_cast<cudaError_t>(status));

@@ -42,6 +42,7 @@ struct GatherArgs {
     int chunk, valid;
     const int32_t* chunk_valid;
     int slice_cols, n_slices;
+    int inputs_ready;  // the index and weight rows predate the preceding kernel: load them before waiting
 };
 
 // A resolved gather launch: the kernel instance, its geometry and every kernel argument.

@@ -21,9 +21,9 @@ SDM_I32, SDM_I64 = 0, 1
 SDM_DEV_TIMEOUT, SDM_DEV_BAD_INDEX = 1, 2
 
 ENTRY_POINTS = ("sdm_decode_step", "sdm_decode_step_ex", "sdm_decode_seq", "sdm_gather", "sdm_gather_kpos",
-                "sdm_gather_plan_init", "sdm_gather_plan_launch", "sdm_status_string", "sdm_device_status",
-                "sdm_version")
-SDM_INPUTS_READY = 1  # sdm_decode_step_ex flag: the inputs predate the kernel launched just before
+                "sdm_gather_plan_init", "sdm_gather_plan_launch", "sdm_gather_plan_launch_ex", "sdm_status_string",
+                "sdm_device_status", "sdm_version")
+SDM_INPUTS_READY = 1  # flag of the _ex calls: the inputs predate the kernel launched just before
 GATHER_PLAN_BYTES = 512  # SDM_GATHER_PLAN_BYTES
 
 _BANK_CODES = {torch.bfloat16: SDM_BF16, torch.float32: SDM_F32}
@@ -72,6 +72,8 @@ def library() -> ctypes.CDLL:
             lib.sdm_gather_plan_init.restype = i32
             lib.sdm_gather_plan_launch.argtypes = [vp, i64, i32, vp]
             lib.sdm_gather_plan_launch.restype = i32
+            lib.sdm_gather_plan_launch_ex.argtypes = [vp, i64, i32, ctypes.c_uint, vp]
+            lib.sdm_gather_plan_launch_ex.restype = i32
             lib.sdm_status_string.argtypes = [i32]
             lib.sdm_status_string.restype = ctypes.c_char_p
             lib.sdm_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint), i32]
@@ -353,11 +355,20 @@ class GatherPlan:
         self._keep = (bank, tuple(tuple(op) for op in ops))
         self.outs, self.device, self.tokens, self.chunk, self.row0_max = outs, dev, tokens, chunk, row0_max
 
-    def launch(self, row0: int, valid: int | None = None, stream=None) -> list:
-        """The planned gather over index rows [row0, row0 + tokens); returns ``outs``."""
-        rc = library().sdm_gather_plan_launch(self._record, row0, self.chunk if valid is None else valid,
-                                              _stream_handle(stream, self.device))
-        _check("sdm_gather_plan_launch", rc)
+    def launch(self, row0: int, valid: int | None = None, stream=None, inputs_ready: bool = False) -> list:
+        """The planned gather over index rows [row0, row0 + tokens); returns ``outs``.
+
+        ``inputs_ready`` (sdm_gather_plan_launch_ex with SDM_INPUTS_READY) promises that those index
+        and weight rows were complete before the kernel enqueued just ahead of this launch began;
+        the launch then reads them and warms L2 with their rows while that kernel still runs."""
+        v = self.chunk if valid is None else valid
+        st = _stream_handle(stream, self.device)
+        if inputs_ready:
+            rc = library().sdm_gather_plan_launch_ex(self._record, row0, v, SDM_INPUTS_READY, st)
+            _check("sdm_gather_plan_launch_ex", rc)
+        else:
+            rc = library().sdm_gather_plan_launch(self._record, row0, v, st)
+            _check("sdm_gather_plan_launch", rc)
         return self.outs
 
 

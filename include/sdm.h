@@ -66,7 +66,7 @@ typedef struct CUstream_st* sdm_stream_t;
 #define SDM_EPLAN (-12)     /* not an initialised gather plan (wrong tag or record size) */
 #define SDM_EROW (-13)      /* row0 outside 0..row0_max, or row0_max + tokens beyond the index rows */
 #define SDM_EDEVICE (-14)   /* the current device is not the one the gather plan was made on */
-#define SDM_EFLAGS (-15)    /* unknown bits in the flags of sdm_decode_step_ex */
+#define SDM_EFLAGS (-15)    /* unknown bits in the flags of an _ex entry point */
 
 /* bits of the device status word */
 #define SDM_DEV_TIMEOUT 1u   /* reserved: a kernel gave up a bounded wait (no current kernel waits) */
@@ -223,6 +223,18 @@ int sdm_gather_plan_init(sdm_gather_plan* plan, const void* bank, int64_t n_slot
  * (nothing launched) or the cudaError_t of a failed launch.
  */
 int sdm_gather_plan_launch(const sdm_gather_plan* plan, int64_t row0, int valid, sdm_stream_t stream);
+
+/*
+ * sdm_gather_plan_launch_ex - sdm_gather_plan_launch with flags; flags == 0 is
+ * sdm_gather_plan_launch. SDM_INPUTS_READY promises that the launch's index and weight rows
+ * [row0, row0 + tokens) were complete before the kernel enqueued just ahead of it on the stream
+ * began: the launch may then read them and warm L2 with the rows they name before it waits for
+ * that kernel (which may still be writing the bank). The bank is read, and the outputs written,
+ * only after the wait; results are the same bits as without the flag. Unknown bits return
+ * SDM_EFLAGS before any other check.
+ */
+int sdm_gather_plan_launch_ex(const sdm_gather_plan* plan, int64_t row0, int valid, unsigned flags,
+                              sdm_stream_t stream);
 
 /* A static string naming a return code of the calls above. */
 const char* sdm_status_string(int status);

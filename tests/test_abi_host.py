@@ -199,6 +199,15 @@ def test_gather_plan_init_null_record(lib):
     assert _plan_init(lib, None) == CODES["SDM_ENULL"]
 
 
+def test_gather_plan_launch_ex_flags(lib):
+    """Unknown flag bits are refused before the record is looked at; the known flag checks as usual."""
+    zero = ctypes.create_string_buffer(sdm.GATHER_PLAN_BYTES)
+    assert lib.sdm_gather_plan_launch_ex(None, 0, 16, 4, None) == CODES["SDM_EFLAGS"]
+    assert lib.sdm_gather_plan_launch_ex(zero, 0, 16, 3, None) == CODES["SDM_EFLAGS"]
+    assert lib.sdm_gather_plan_launch_ex(None, 0, 16, sdm.SDM_INPUTS_READY, None) == CODES["SDM_ENULL"]
+    assert lib.sdm_gather_plan_launch_ex(zero, 0, 16, sdm.SDM_INPUTS_READY, None) == CODES["SDM_EPLAN"]
+
+
 def test_gather_plan_launch_refuses_a_foreign_record(lib):
     zero = ctypes.create_string_buffer(sdm.GATHER_PLAN_BYTES)
     assert lib.sdm_gather_plan_launch(zero, 0, 16, None) == CODES["SDM_EPLAN"]

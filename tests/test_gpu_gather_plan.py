@@ -120,3 +120,36 @@ def test_empty_plan_launches_nothing():
     plan = sdm.GatherPlan(g["bank"], g["ops"], tokens=0, chunk=8, outs=outs)
     plan.launch(40, 0)
     torch.cuda.synchronize()
+
+
+def test_flagged_launches_after_decode_steps_see_their_writes():
+    """Plan launches with SDM_INPUTS_READY (the index and weight rows were made up front) chained
+    after decode steps that rewrite the very rows they gather: each launch may warm L2 with its
+    rows while the step ahead still writes them, and must still read the written rows. The same
+    sequence without the flag (checked against the oracle above) gives the reference bits."""
+    from parity import DECODE_KEYS
+
+    S, P, hd, W, T = 16, 64, 128, 32, 6
+    dwl = workloads.DecodeWorkload("plan_after_decode", "bf16", S, hd, P, W, W, 1, T, "i32", 0.35, bank_std=0.5,
+                                   seed=21)
+    x = workloads.make_decode_inputs(dwl, device=DEV)
+    gen = torch.Generator(device=DEV)
+    gen.manual_seed(22)
+    rows, tokens, chunk = 6 * 64, 64, 16
+    ops = [(torch.randint(0, S * P, (rows, w), generator=gen, device=DEV, dtype=torch.int32),
+            (torch.randn((rows, w), generator=gen, device=DEV) * 0.125).to(torch.bfloat16)) for w in (48, 16)]
+    results = []
+    for flag in (False, True):
+        bank = x["bank"].clone()
+        plan = sdm.GatherPlan(bank, ops, tokens=tokens, chunk=chunk)
+        got = []
+        for t in range(T):
+            sdm.decode_step(bank, *(x[k][t] for k in DECODE_KEYS))
+            outs = plan.launch(t * 64, chunk - t, inputs_ready=flag)
+            got.append([o.clone() for o in outs])
+        torch.cuda.synchronize()
+        results.append((got, bank))
+    (plain, bank_p), (flagged, bank_f) = results
+    assert bits_equal(to_np(bank_p), to_np(bank_f))
+    for a, b in zip(plain, flagged):
+        assert bits_equal(to_np(a[0]), to_np(b[0])) and bits_equal(to_np(a[1]), to_np(b[1]))
