@@ -378,9 +378,12 @@ __global__ void __launch_bounds__(kMaxThreads, 2) decode_vec_kernel(const Decode
     // With inputs_ready the inputs predate the preceding kernel: token 0's metadata is read and its
     // rows are warmed in L2 before waiting for that kernel; the bank is read and written (and `out`
     // written) only after the wait. L2 is the point of coherence, so a line warmed early still
-    // holds every later write to it.
-    if (!a.inputs_ready) grid_dependency_wait();
-    if (early_trigger) grid_launch_dependents();
+    // holds every later write to it. The next launch is released only after the wait, so at most
+    // one launch runs its early part ahead of the kernel that is working.
+    if (!a.inputs_ready) {
+        grid_dependency_wait();
+        if (early_trigger) grid_launch_dependents();
+    }
     prefetch_meta<I>(a, s, L, smem);  // token 0
     cp_async_wait_all();
     __syncthreads();
@@ -393,6 +396,7 @@ __global__ void __launch_bounds__(kMaxThreads, 2) decode_vec_kernel(const Decode
         prefetch_rows_l2(bank, koff, W, row_bytes);
         prefetch_rows_l2(bank, qoff, R, row_bytes);
         grid_dependency_wait();
+        if (early_trigger) grid_launch_dependents();
     }
 
     for (int t = 0; t < a.T; ++t) {
@@ -609,9 +613,12 @@ __global__ void __launch_bounds__(128, 7) decode_vec1_kernel(const DecodeArgs a,
     // With inputs_ready the inputs predate the preceding kernel: token 0's metadata is read and its
     // rows are warmed in L2 before waiting for that kernel; the bank is read and written (and `out`
     // written) only after the wait. L2 is the point of coherence, so a line warmed early still
-    // holds every later write to it.
-    if (!a.inputs_ready) grid_dependency_wait();
-    if (early_trigger) grid_launch_dependents();
+    // holds every later write to it. The next launch is released only after the wait, so at most
+    // one launch runs its early part ahead of the kernel that is working.
+    if (!a.inputs_ready) {
+        grid_dependency_wait();
+        if (early_trigger) grid_launch_dependents();
+    }
     prefetch_meta<I>(a, s, L, smem);  // token 0
     cp_async_wait_all();
     __syncthreads();
@@ -624,6 +631,7 @@ __global__ void __launch_bounds__(128, 7) decode_vec1_kernel(const DecodeArgs a,
         prefetch_rows_l2(bank, koff, W, row_bytes);
         prefetch_rows_l2(bank, qoff, R, row_bytes);
         grid_dependency_wait();
+        if (early_trigger) grid_launch_dependents();
     }
 
     for (int t = 0; t < a.T; ++t) {
@@ -808,9 +816,12 @@ __global__ void __launch_bounds__(kMaxThreads, 1) decode_stream_kernel(const Dec
     // With inputs_ready the inputs predate the preceding kernel: token 0's metadata is read and its
     // rows are warmed in L2 before waiting for that kernel; the bank is read and written (and `out`
     // written) only after the wait. L2 is the point of coherence, so a line warmed early still
-    // holds every later write to it.
-    if (!a.inputs_ready) grid_dependency_wait();
-    if (early_trigger) grid_launch_dependents();
+    // holds every later write to it. The next launch is released only after the wait, so at most
+    // one launch runs its early part ahead of the kernel that is working.
+    if (!a.inputs_ready) {
+        grid_dependency_wait();
+        if (early_trigger) grid_launch_dependents();
+    }
     prefetch_meta<I>(a, s, L, smem);  // token 0
     cp_async_wait_all();
     __syncthreads();
@@ -823,6 +834,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) decode_stream_kernel(const Dec
         prefetch_rows_l2(bank, koff, W, row_bytes);
         prefetch_rows_l2(bank, qoff, R, row_bytes);
         grid_dependency_wait();
+        if (early_trigger) grid_launch_dependents();
     }
 
     for (int t = 0; t < a.T; ++t) {
@@ -952,8 +964,10 @@ __global__ void __launch_bounds__(kMaxThreads, 1) decode_stream1_kernel(const De
         return reinterpret_cast<const float*>(ring + st * stage_bytes)[r * sw + tid];
     };
 
-    if (!a.inputs_ready) grid_dependency_wait();  // as in decode_stream_kernel
-    if (early_trigger) grid_launch_dependents();
+    if (!a.inputs_ready) {  // as in decode_stream_kernel
+        grid_dependency_wait();
+        if (early_trigger) grid_launch_dependents();
+    }
     prefetch_meta<I>(a, s, L, smem);  // token 0
     cp_async_wait_all();
     __syncthreads();
@@ -966,6 +980,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) decode_stream1_kernel(const De
         prefetch_rows_l2(bank, koff, W, row_bytes);
         prefetch_rows_l2(bank, qoff, R, row_bytes);
         grid_dependency_wait();
+        if (early_trigger) grid_launch_dependents();
     }
 
     for (int t = 0; t < a.T; ++t) {

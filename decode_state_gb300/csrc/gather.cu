@@ -100,12 +100,19 @@ __global__ void __launch_bounds__(kMaxThreads) gather_kernel(const GatherArgs a,
     // With inputs_ready the index and weight rows predate the preceding kernel: they are read, and
     // the rows they name warmed in L2, before waiting for that kernel; the bank is read and the
     // outputs written only after the wait (L2 is the point of coherence: a line warmed early still
-    // holds every later write to it).
-    if (!a.inputs_ready) grid_dependency_wait();
-    if (early_trigger) grid_launch_dependents();
+    // holds every later write to it). The next launch is released only after the wait: released
+    // at the start, whole chains of launches would sit waiting with their rows warmed far ahead
+    // (a walk of plan slabs from a graph measured 6.1 instead of 3.9 us per launch).
+    if (!a.inputs_ready) {
+        grid_dependency_wait();
+        if (early_trigger) grid_launch_dependents();
+    }
     const int vt = a.chunk_valid != nullptr ? __ldg(a.chunk_valid + t / a.chunk) : a.valid;
     if ((int)(t % a.chunk) >= vt) {
-        if (a.inputs_ready) grid_dependency_wait();
+        if (a.inputs_ready) {
+            grid_dependency_wait();
+            if (early_trigger) grid_launch_dependents();
+        }
         write_padding<E>(a, t, c0, ncols, j, active, stash_bulk && a.n_slices == 1);
         return;
     }
@@ -142,6 +149,7 @@ __global__ void __launch_bounds__(kMaxThreads) gather_kernel(const GatherArgs a,
             if (slot[e] >= 0) asm volatile("prefetch.global.L2 [%0];" ::"l"(src + slot[e] * rowb + (int64_t)l * 128));
         }
         grid_dependency_wait();
+        if (early_trigger) grid_launch_dependents();
     }
 
     if (BULK) {
