@@ -2,11 +2,12 @@
  * sdm.h - C ABI of the GB300 (sm_103a) sparse delta-memory (SDM) decode-state library.
  *
  * Three operations, each one kernel launch on the caller's stream:
- *   sdm_decode_step  one write-then-read token for every stream
+ *   sdm_decode_step  one write-then-read token for every stream (sdm_decode_step_ex: with flags)
  *   sdm_decode_seq   T tokens for every stream in one persistent launch
  *   sdm_gather       per-token weighted sums of bank rows (one or two operands), optional stash
  *                    (sdm_gather_kpos: with a compact snapshot instead; sdm_gather_plan_*: a
- *                    checked launch, replayed per slab of an index tensor)
+ *                    checked launch, replayed per slab of an index tensor; _launch_ex: with
+ *                    flags)
  *
  * Common rules
  *   - Every pointer argument except `stream` (and the host records and arrays named as such) is a
@@ -23,7 +24,9 @@
  *     SDM_DEV_BAD_INDEX in the device status word (sdm_device_status).
  *   - Launches use programmatic stream serialization: a kernel may be scheduled while the previous
  *     kernel on the stream is still finishing, but it reads and writes no memory before that kernel
- *     has completed (griddepcontrol.wait), so stream order is kept.
+ *     has completed (griddepcontrol.wait), so stream order is kept. The one exception is opt-in:
+ *     with SDM_INPUTS_READY an _ex call may read its inputs (never the bank, never its outputs)
+ *     and warm L2 before that wait, on the caller's promise that those inputs are already final.
  *   - bfloat16 data is raw 16-bit patterns (the high half of an IEEE float32).
  *   - Results are deterministic: every sum is accumulated in a fixed order independent of the GPU.
  *
