@@ -227,6 +227,18 @@ def oracle_gather_tokens(bank_h, g: dict, tokens, chunk: int):
     return len(tokens), time.perf_counter() - t0
 
 
+def decode_config(wl, r: sdist.Rank, call: str) -> dict:
+    """The config object of a decode workload's JSON line; both arms use it, so that they name the
+    same workload with the same keys (only `call` differs)."""
+    bank_gib = wl.n_slots * wl.hd * (2 if wl.bank_dtype == "bf16" else 4) / 2 ** 30
+    return {"workload": wl.name, "streams": wl.n_streams, "head_dim": wl.hd,
+            "slots_per_stream": wl.slots_per_stream, "W": wl.W, "R": wl.R, "G": wl.G, "T": wl.T,
+            "bank_dtype": wl.bank_dtype, "idx_dtype": wl.idx_dtype, "call": call,
+            "l2": (f"inputs larger than L2 ({bank_gib:.2f} GiB bank), no flush" if bank_gib > 0.2 else
+                   f"L2-resident ({bank_gib * 1024:.0f} MiB bank)"),
+            "parallelism": f"weak: {r.world} independent shard(s), no collective in the data path"}
+
+
 class Case:
     """One timed workload: its step, its units and bytes, its end-to-end form and its oracle."""
 
@@ -290,13 +302,7 @@ class Case:
                     "chunk": wl.chunk, "widths": list(wl.widths), "bank_dtype": wl.bank_dtype,
                     "idx_dtype": wl.idx_dtype, "w_dtype": wl.w_dtype, "stash": wl.stash, "call": "sdm_gather",
                     "l2": f"inputs larger than L2 ({gib:.0f} GiB bank), no flush", "parallelism": par}
-        bank_gib = wl.n_slots * wl.hd * (2 if wl.bank_dtype == "bf16" else 4) / 2 ** 30
-        return {"workload": wl.name, "streams": wl.n_streams, "head_dim": wl.hd,
-                "slots_per_stream": wl.slots_per_stream, "W": wl.W, "R": wl.R, "G": wl.G, "T": wl.T,
-                "bank_dtype": wl.bank_dtype, "idx_dtype": wl.idx_dtype,
-                "call": "sdm_decode_seq" if self.kind == "decode_seq" else "sdm_decode_step x T",
-                "l2": (f"inputs larger than L2 ({bank_gib:.2f} GiB bank), no flush" if bank_gib > 0.2 else
-                       f"L2-resident ({bank_gib * 1024:.0f} MiB bank)"), "parallelism": par}
+        return decode_config(wl, r, "sdm_decode_seq" if self.kind == "decode_seq" else "sdm_decode_step x T")
 
     # end to end: host inputs in, results out, every step
     def e2e(self, steps: int, r: sdist.Rank) -> dict:
@@ -688,10 +694,7 @@ def run_reference(args, r: sdist.Rank):
     return {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": r.world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs * 1e3 / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-            "config": {"workload": base.name, "streams": base.n_streams, "head_dim": base.hd,
-                       "slots_per_stream": base.slots_per_stream, "W": base.W, "R": base.R, "G": base.G,
-                       "T": base.T, "bank_dtype": base.bank_dtype, "idx_dtype": base.idx_dtype,
-                       "call": "oracle_sdm_decode_seq"},
+            "config": decode_config(base, r, "oracle_sdm_decode_seq"),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 

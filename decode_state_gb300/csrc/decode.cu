@@ -1181,6 +1181,8 @@ int launch_typed(int path, bool scalar, const DecodeArgs& a, dim3 grid, dim3 blo
                                    : (a.stream_stages == 3 ? decode_stream_kernel<E, I, 3>
                                                            : decode_stream_kernel<E, I, 4>))
                                           : decode_simt_kernel<E, I>;
+    const int rc = allow_smem(reinterpret_cast<const void*>(kernel), smem);  // before the occupancy query
+    if (rc != 0) return rc;
     const int early = fits_one_wave(kernel, grid.x, (int)block.x, smem) ? 1 : 0;
     return launch_pdl(kernel, grid, block, smem, stream, a, early);
 }

@@ -304,7 +304,13 @@ int plan_gather(const GatherArgs& a0, int bank_dtype, int idx_dtype, int w_dtype
         else
             resolve_w<float, int64_t>(w_dtype, bulk, L);
     }
-    // the early trigger only when every block of this launch is resident at once
+    // the early trigger only when every block of this launch is resident at once; the shared-memory
+    // limit is raised first, so that the occupancy query sees the launch's own limit
+    const int rc = allow_smem(L->fn, L->smem);
+    if (rc != 0) {
+        *L = GatherLaunch{};
+        return rc;
+    }
     int per_sm = 0;
     cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, L->fn, (int)L->block, L->smem);
     if (e != cudaSuccess) {

@@ -344,6 +344,14 @@ const char* sdm_status_string(int status) {
 
 int sdm_device_status(unsigned int* status, int clear) {
     if (!status) return SDM_ENULL;
+    // every kernel of the device, on any stream, has finished before the words are read (and
+    // cleared): the symbol copies below are ordered only on the legacy default stream
+    const cudaError_t s = cudaDeviceSynchronize();
+    if (s != cudaSuccess) {
+        (void)cudaGetLastError();
+        *status = 0;
+        return (int)s;
+    }
     unsigned int a = 0, b = 0;
     int e = sdm::decode_status(&a, clear != 0);
     if (e == 0) e = sdm::gather_status(&b, clear != 0);

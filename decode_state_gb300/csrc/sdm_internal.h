@@ -72,17 +72,22 @@ int sm_count();
 size_t smem_per_sm();
 size_t smem_reserved_per_block();
 
+// Let `kernel` use `smem` bytes of dynamic shared memory (raises the limit above the default 48 KB
+// on the current device). Called before any occupancy query of that launch, so that the query sees
+// the launch's real limit. Returns a cudaError_t.
+inline int allow_smem(const void* kernel, size_t smem) {
+    if (smem <= 48 * 1024) return 0;
+    const cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) (void)cudaGetLastError();
+    return (int)e;
+}
+
 // Launch the kernel at address `kernel` (arguments as an array of pointers to them) with
-// programmatic stream serialization (see grid_dependency_wait). Returns a cudaError_t. Raises the
-// dynamic shared-memory limit first when smem exceeds the default 48 KB.
+// programmatic stream serialization (see grid_dependency_wait). The dynamic shared-memory limit
+// must already allow `smem` (allow_smem). Returns the cudaError_t of the launch call itself; the
+// error state of the runtime is consumed only when that call failed, so an earlier error left by
+// other code is neither reported nor cleared here.
 inline int launch_pdl_raw(const void* kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t stream, void** args) {
-    if (smem > 48 * 1024) {
-        const cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) {
-            (void)cudaGetLastError();
-            return (int)e;
-        }
-    }
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
@@ -93,9 +98,8 @@ inline int launch_pdl_raw(const void* kernel, dim3 grid, dim3 block, size_t smem
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelExC(&cfg, kernel, args);
-    if (e == cudaSuccess) e = cudaGetLastError();
-    else (void)cudaGetLastError();
+    const cudaError_t e = cudaLaunchKernelExC(&cfg, kernel, args);
+    if (e != cudaSuccess) (void)cudaGetLastError();
     return (int)e;
 }
 

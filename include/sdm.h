@@ -211,7 +211,8 @@ typedef struct sdm_gather_plan {
  *   rows       index rows the arrays hold; row0_max >= 0 with row0_max + tokens <= rows
  *   tokens, chunk  tokens per launch (>= 0, a multiple of chunk), chunk >= 1
  * Other arguments as sdm_gather. Returns 0, an SDM_E* code, or a cudaError_t from the device
- * queries (current device, multiprocessor count, occupancy).
+ * queries and settings (current device, multiprocessor count, the kernel's shared-memory limit,
+ * occupancy).
  */
 int sdm_gather_plan_init(sdm_gather_plan* plan, const void* bank, int64_t n_slots, int hd, int bank_dtype, int n_ops,
                          const void* const idx[2], const void* const w[2], float* const out[2], const int width[2],
@@ -244,8 +245,10 @@ const char* sdm_status_string(int status);
 
 /*
  * sdm_device_status - read (and, if clear != 0, reset) the device status word of the current
- * device: an OR of SDM_DEV_* bits raised by kernels since the last reset. Synchronises the
- * device; not for use inside graph capture. Returns 0 or a cudaError_t; *status receives the word.
+ * device: an OR of SDM_DEV_* bits raised by kernels since the last reset. Synchronises the whole
+ * device first (cudaDeviceSynchronize), so that the kernels of every stream, non-blocking streams
+ * included, have finished before the word is read or cleared; not for use inside graph capture.
+ * Returns 0 or a cudaError_t (then *status is 0); *status receives the word.
  */
 int sdm_device_status(unsigned int* status, int clear);
 

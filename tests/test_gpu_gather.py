@@ -125,6 +125,23 @@ def test_gather_out_of_range_index_is_skipped_and_flagged():
     assert bits_equal(to_np(stash), rs)
 
 
+def test_device_status_waits_for_side_streams():
+    """sdm_device_status synchronises the device: a gather still running on a non-blocking side
+    stream has raised its bit before the word is read, with no synchronisation by the caller."""
+    wl = _gw("bf16", "bf16", "i64", 1 << 16, 128, 4096, 64, (64, 64), True, False, seed=11)
+    g = workloads.make_gather_inputs(wl, device=DEV)
+    idx, w = g["ops"][0]
+    idx[wl.tokens - 1, wl.widths[0] - 1] = -5  # the very last entry of the launch
+    torch.cuda.synchronize()
+    sdm.device_status(clear=True)
+    side = torch.cuda.Stream(DEV)
+    with torch.cuda.stream(side):
+        for _ in range(4):  # several launches queued behind one another on the side stream
+            sdm.gather(g["bank"], [(idx, w), g["ops"][1]], chunk=wl.chunk)
+    assert sdm.device_status(clear=True) & sdm.SDM_DEV_BAD_INDEX
+    assert sdm.device_status(clear=True) == 0  # cleared after every launch had finished
+
+
 @pytest.mark.parametrize("wl", [workloads.C4, workloads.C4_BWD], ids=lambda w: w.name)
 def test_gather_full_size(wl):
     """A full gather workload in the benchmark's launch configuration (the two-operand forward
