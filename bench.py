@@ -258,9 +258,12 @@ class Case:
             self.x = workloads.make_decode_inputs(wl, device=dev, seed=sdist.shard_seed(wl.seed, r))
             bdt = workloads.BANK_DTYPES[wl.bank_dtype]
             self.out = torch.empty((wl.T, wl.n_streams, wl.hd), dtype=bdt, device=dev)
+            if self.kind == "decode_seq_stream_major":  # the prompt's own layout [S, T, .], made once
+                self.x = {k: (v.transpose(0, 1).contiguous() if k in DECODE_KEYS else v) for k, v in self.x.items()}
+                self.out = torch.empty((wl.n_streams, wl.T, wl.hd), dtype=bdt, device=dev)
             self.units = wl.n_streams * wl.T
             self.unit = UNIT
-            self.launches = 1 if wl.mode == "seq" else wl.T
+            self.launches = 1 if wl.mode.startswith("seq") else wl.T
             self.nbytes = workloads.decode_bytes_per_stream_token(wl) * wl.n_streams * wl.T
             self.kernel = f"decode_vec_kernel<{wl.bank_dtype},{wl.idx_dtype}>"
             self.metric = METRIC
@@ -286,6 +289,8 @@ class Case:
         wl, sdm = self.wl, self.sdm
         if self.kind == "decode_seq":
             sdm.decode_seq(self.x["bank"], *(self.x[k] for k in DECODE_KEYS), out=self.out)
+        elif self.kind == "decode_seq_stream_major":
+            sdm.decode_seq(self.x["bank"], *(self.x[k] for k in DECODE_KEYS), out=self.out, stream_major=True)
         elif self.kind == "decode_step":
             for t in range(wl.T):
                 sdm.decode_step(self.x["bank"], *(self.x[k][t] for k in DECODE_KEYS), out=self.out[t])
@@ -302,7 +307,9 @@ class Case:
                     "chunk": wl.chunk, "widths": list(wl.widths), "bank_dtype": wl.bank_dtype,
                     "idx_dtype": wl.idx_dtype, "w_dtype": wl.w_dtype, "stash": wl.stash, "call": "sdm_gather",
                     "l2": f"inputs larger than L2 ({gib:.0f} GiB bank), no flush", "parallelism": par}
-        return decode_config(wl, r, "sdm_decode_seq" if self.kind == "decode_seq" else "sdm_decode_step x T")
+        call = {"decode_seq": "sdm_decode_seq", "decode_seq_stream_major": "sdm_decode_seq_ex (SDM_STREAM_MAJOR)",
+                "decode_step": "sdm_decode_step x T"}[self.kind]
+        return decode_config(wl, r, call)
 
     # end to end: host inputs in, results out, every step
     def e2e(self, steps: int, r: sdist.Rank) -> dict:
@@ -344,6 +351,8 @@ class Case:
                     d.copy_(h, non_blocking=True)
                 if self.kind == "decode_seq":
                     sdm.decode_seq(self.x["bank"], *dev_in, out=self.out)
+                elif self.kind == "decode_seq_stream_major":
+                    sdm.decode_seq(self.x["bank"], *dev_in, out=self.out, stream_major=True)
                 else:
                     for t in range(wl.T):
                         sdm.decode_step(self.x["bank"], *(d[t] for d in dev_in), out=self.out[t])
@@ -387,8 +396,11 @@ class Case:
             S, P = self.wl.n_streams, self.wl.slots_per_stream
             order = torch.randperm(S, generator=torch.Generator().manual_seed(0)).tolist()
             done, secs, n = 0, 0.0, 0
+            xt = self.x  # the oracle takes time-major arrays: a stream-major case is viewed back
+            if self.kind == "decode_seq_stream_major":
+                xt = {k: (v.transpose(0, 1) if k in DECODE_KEYS else v) for k, v in self.x.items()}
             for s in order:
-                d, t = oracle_stream_tokens(self.x, [s], P)
+                d, t = oracle_stream_tokens(xt, [s], P)
                 done, secs, n = done + d, secs + t, n + 1
                 if secs >= budget_s:
                     break

@@ -384,7 +384,7 @@ __global__ void __launch_bounds__(kMaxThreads, 2) decode_vec_kernel(const Decode
         grid_dependency_wait();
         if (early_trigger) grid_launch_dependents();
     }
-    prefetch_meta<I>(a, s, L, smem);  // token 0
+    prefetch_meta<I>(a, s * a.sstride, L, smem);  // token 0
     cp_async_wait_all();
     __syncthreads();
     if (G == 1 && tid == 0)
@@ -400,7 +400,7 @@ __global__ void __launch_bounds__(kMaxThreads, 2) decode_vec_kernel(const Decode
     }
 
     for (int t = 0; t < a.T; ++t) {
-        const int64_t ts = (int64_t)t * a.n_streams + s;  // (token, stream) row of the time-major inputs
+        const int64_t ts = (int64_t)t * a.tstride + s * a.sstride;  // (token, stream) row of the inputs
 
         // 1. the write rows; the next token's metadata meanwhile
         ldgsts_rows<E>(rows, bank, koff, W, sw, row_bytes);
@@ -420,9 +420,9 @@ __global__ void __launch_bounds__(kMaxThreads, 2) decode_vec_kernel(const Decode
         const uint64_t dsh = dw2[0];
         const bool more = t + 1 < a.T;
         if (more) {
-            prefetch_meta<I>(a, ts + a.n_streams, L, smem);
+            prefetch_meta<I>(a, ts + a.tstride, L, smem);
             if (G == 1 && tid == 0)  // the next token's shared gate, while this token's rows are in flight
-                *reinterpret_cast<float*>(smem + L.dnext) = gate(__ldg(a.g + ts + a.n_streams));
+                *reinterpret_cast<float*>(smem + L.dnext) = gate(__ldg(a.g + ts + a.tstride));
         }
         if (more)
             asm volatile("cp.async.wait_group 1;" ::: "memory");  // the rows, not yet the metadata
@@ -619,7 +619,7 @@ __global__ void __launch_bounds__(128, 7) decode_vec1_kernel(const DecodeArgs a,
         grid_dependency_wait();
         if (early_trigger) grid_launch_dependents();
     }
-    prefetch_meta<I>(a, s, L, smem);  // token 0
+    prefetch_meta<I>(a, s * a.sstride, L, smem);  // token 0
     cp_async_wait_all();
     __syncthreads();
     if (G == 1 && tid == 0)
@@ -635,7 +635,7 @@ __global__ void __launch_bounds__(128, 7) decode_vec1_kernel(const DecodeArgs a,
     }
 
     for (int t = 0; t < a.T; ++t) {
-        const int64_t ts = (int64_t)t * a.n_streams + s;
+        const int64_t ts = (int64_t)t * a.tstride + s * a.sstride;
 
         ldgsts_rows<E>(rows, bank, koff, W, sw, row_bytes);
         {
@@ -650,9 +650,9 @@ __global__ void __launch_bounds__(128, 7) decode_vec1_kernel(const DecodeArgs a,
         const float dsh = f2lo(dw2[0]);
         const bool more = t + 1 < a.T;
         if (more) {
-            prefetch_meta<I>(a, ts + a.n_streams, L, smem);
+            prefetch_meta<I>(a, ts + a.tstride, L, smem);
             if (G == 1 && tid == 0)
-                *reinterpret_cast<float*>(smem + L.dnext) = gate(__ldg(a.g + ts + a.n_streams));
+                *reinterpret_cast<float*>(smem + L.dnext) = gate(__ldg(a.g + ts + a.tstride));
         }
         if (more)
             asm volatile("cp.async.wait_group 1;" ::: "memory");
@@ -822,7 +822,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) decode_stream_kernel(const Dec
         grid_dependency_wait();
         if (early_trigger) grid_launch_dependents();
     }
-    prefetch_meta<I>(a, s, L, smem);  // token 0
+    prefetch_meta<I>(a, s * a.sstride, L, smem);  // token 0
     cp_async_wait_all();
     __syncthreads();
     if (G == 1 && tid == 0)
@@ -838,7 +838,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) decode_stream_kernel(const Dec
     }
 
     for (int t = 0; t < a.T; ++t) {
-        const int64_t ts = (int64_t)t * a.n_streams + s;
+        const int64_t ts = (int64_t)t * a.tstride + s * a.sstride;
         uint64_t vr = 0;
         if (active) {
             const float2 vv = __ldg(reinterpret_cast<const float2*>(a.v + ts * hd + c0 + j));
@@ -893,9 +893,9 @@ __global__ void __launch_bounds__(kMaxThreads, 1) decode_stream_kernel(const Dec
         // pass 3: the read rows, after every write of this token; the next token's metadata too
         const bool more = t + 1 < a.T;
         if (more) {
-            prefetch_meta<I>(a, ts + a.n_streams, L, smem);
+            prefetch_meta<I>(a, ts + a.tstride, L, smem);
             if (G == 1 && tid == 0)
-                *reinterpret_cast<float*>(smem + L.dnext) = gate(__ldg(a.g + ts + a.n_streams));
+                *reinterpret_cast<float*>(smem + L.dnext) = gate(__ldg(a.g + ts + a.tstride));
         }
         uint64_t racc = 0;
         for (int q = 0; q < NS - 1; ++q) {
@@ -968,7 +968,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) decode_stream1_kernel(const De
         grid_dependency_wait();
         if (early_trigger) grid_launch_dependents();
     }
-    prefetch_meta<I>(a, s, L, smem);  // token 0
+    prefetch_meta<I>(a, s * a.sstride, L, smem);  // token 0
     cp_async_wait_all();
     __syncthreads();
     if (G == 1 && tid == 0)
@@ -984,7 +984,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) decode_stream1_kernel(const De
     }
 
     for (int t = 0; t < a.T; ++t) {
-        const int64_t ts = (int64_t)t * a.n_streams + s;
+        const int64_t ts = (int64_t)t * a.tstride + s * a.sstride;
         const float vr = active ? __ldg(a.v + ts * hd + c0 + j) : 0.0f;
         const float beta = *reinterpret_cast<const float*>(smem + L.beta);
         const float dsh = f2lo(dw2[0]);
@@ -1027,9 +1027,9 @@ __global__ void __launch_bounds__(kMaxThreads, 1) decode_stream1_kernel(const De
 
         const bool more = t + 1 < a.T;
         if (more) {
-            prefetch_meta<I>(a, ts + a.n_streams, L, smem);
+            prefetch_meta<I>(a, ts + a.tstride, L, smem);
             if (G == 1 && tid == 0)
-                *reinterpret_cast<float*>(smem + L.dnext) = gate(__ldg(a.g + ts + a.n_streams));
+                *reinterpret_cast<float*>(smem + L.dnext) = gate(__ldg(a.g + ts + a.tstride));
         }
         float racc = 0.0f;
         for (int q = 0; q < NS - 1; ++q) {
@@ -1119,7 +1119,7 @@ __global__ void __launch_bounds__(kMaxThreads) decode_simt_kernel(const DecodeAr
     if (early_trigger) grid_launch_dependents();
 
     for (int t = 0; t < a.T; ++t) {
-        const int64_t ts = (int64_t)t * a.n_streams + s;
+        const int64_t ts = (int64_t)t * a.tstride + s * a.sstride;
         for (int i = tid; i < W; i += nt) {
             const int64_t e = ts * W + i;
             k_slot[i] = load_index<I>(a.k_idx, e);

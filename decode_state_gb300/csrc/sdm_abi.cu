@@ -95,7 +95,8 @@ int check_decode(void* bank, const void* k_idx, const float* k_val, const float*
 
 int decode_common(void* bank, const void* k_idx, const float* k_val, const float* v, const float* beta,
                   const float* g, const void* q_idx, const float* q_val, void* out, int64_t n_streams, int hd, int W,
-                  int R, int G, int T, int bank_dtype, int idx_dtype, int inputs_ready, sdm_stream_t stream) {
+                  int R, int G, int T, int bank_dtype, int idx_dtype, int inputs_ready, bool stream_major,
+                  sdm_stream_t stream) {
     const int rc = check_decode(bank, k_idx, k_val, v, beta, g, q_idx, q_val, out, n_streams, hd, W, R, G, T,
                                 bank_dtype, idx_dtype);
     if (rc != SDM_OK || n_streams == 0 || T == 0) return rc;
@@ -115,6 +116,8 @@ int decode_common(void* bank, const void* k_idx, const float* k_val, const float
     a.R = R;
     a.G = G;
     a.T = T;
+    a.tstride = stream_major ? 1 : n_streams;
+    a.sstride = stream_major ? T : 1;
     a.inputs_ready = inputs_ready;
     return sdm::launch_decode(a, bank_dtype, idx_dtype, reinterpret_cast<cudaStream_t>(stream));
 }
@@ -127,14 +130,22 @@ int sdm_decode_seq(void* bank, const void* k_idx, const float* k_val, const floa
                    const float* g, const void* q_idx, const float* q_val, void* out, int64_t n_streams, int hd,
                    int W, int R, int G, int T, int bank_dtype, int idx_dtype, sdm_stream_t stream) {
     return decode_common(bank, k_idx, k_val, v, beta, g, q_idx, q_val, out, n_streams, hd, W, R, G, T, bank_dtype,
-                         idx_dtype, 0, stream);
+                         idx_dtype, 0, false, stream);
+}
+
+int sdm_decode_seq_ex(void* bank, const void* k_idx, const float* k_val, const float* v, const float* beta,
+                      const float* g, const void* q_idx, const float* q_val, void* out, int64_t n_streams, int hd,
+                      int W, int R, int G, int T, int bank_dtype, int idx_dtype, unsigned flags, sdm_stream_t stream) {
+    if (flags & ~(SDM_INPUTS_READY | SDM_STREAM_MAJOR)) return SDM_EFLAGS;
+    return decode_common(bank, k_idx, k_val, v, beta, g, q_idx, q_val, out, n_streams, hd, W, R, G, T, bank_dtype,
+                         idx_dtype, (flags & SDM_INPUTS_READY) ? 1 : 0, (flags & SDM_STREAM_MAJOR) != 0, stream);
 }
 
 int sdm_decode_step(void* bank, const void* k_idx, const float* k_val, const float* v, const float* beta,
                     const float* g, const void* q_idx, const float* q_val, void* out, int64_t n_streams, int hd,
                     int W, int R, int G, int bank_dtype, int idx_dtype, sdm_stream_t stream) {
     return decode_common(bank, k_idx, k_val, v, beta, g, q_idx, q_val, out, n_streams, hd, W, R, G, 1, bank_dtype,
-                         idx_dtype, 0, stream);
+                         idx_dtype, 0, false, stream);
 }
 
 int sdm_decode_step_ex(void* bank, const void* k_idx, const float* k_val, const float* v, const float* beta,
@@ -142,7 +153,7 @@ int sdm_decode_step_ex(void* bank, const void* k_idx, const float* k_val, const 
                        int W, int R, int G, int bank_dtype, int idx_dtype, unsigned flags, sdm_stream_t stream) {
     if (flags & ~SDM_INPUTS_READY) return SDM_EFLAGS;
     return decode_common(bank, k_idx, k_val, v, beta, g, q_idx, q_val, out, n_streams, hd, W, R, G, 1, bank_dtype,
-                         idx_dtype, (flags & SDM_INPUTS_READY) ? 1 : 0, stream);
+                         idx_dtype, (flags & SDM_INPUTS_READY) ? 1 : 0, false, stream);
 }
 
 }  // extern "C"

@@ -19,6 +19,9 @@ struct DecodeArgs {
     void* out;
     int64_t n_streams;
     int hd, W, R, G, T;
+    // the inputs' row of (token t, stream s) is t * tstride + s * sstride, and so is the readings'
+    // row: time-major [T, S, .] has (S, 1), the stream-major layout [S, T, .] has (1, T)
+    int64_t tstride, sstride;
     int slice_cols;   // columns one block owns (the last slice may be narrower)
     int n_slices;     // ceil(hd / slice_cols)
     int stream_rows;    // rows per ring chunk of the streaming path

@@ -20,10 +20,12 @@ SDM_BF16, SDM_F32 = 0, 1
 SDM_I32, SDM_I64 = 0, 1
 SDM_DEV_TIMEOUT, SDM_DEV_BAD_INDEX = 1, 2
 
-ENTRY_POINTS = ("sdm_decode_step", "sdm_decode_step_ex", "sdm_decode_seq", "sdm_gather", "sdm_gather_kpos",
+ENTRY_POINTS = ("sdm_decode_step", "sdm_decode_step_ex", "sdm_decode_seq", "sdm_decode_seq_ex", "sdm_gather",
+                "sdm_gather_kpos",
                 "sdm_gather_plan_init", "sdm_gather_plan_launch", "sdm_gather_plan_launch_ex", "sdm_status_string",
                 "sdm_device_status", "sdm_version")
 SDM_INPUTS_READY = 1  # flag of the _ex calls: the inputs predate the kernel launched just before
+SDM_STREAM_MAJOR = 2  # flag of sdm_decode_seq_ex: per-token arrays are [S, T, .] instead of [T, S, .]
 GATHER_PLAN_BYTES = 512  # SDM_GATHER_PLAN_BYTES
 
 _BANK_CODES = {torch.bfloat16: SDM_BF16, torch.float32: SDM_F32}
@@ -60,6 +62,8 @@ def library() -> ctypes.CDLL:
             lib.sdm_decode_step_ex.restype = i32
             lib.sdm_decode_seq.argtypes = dec + [i32, i32, i32, vp]
             lib.sdm_decode_seq.restype = i32
+            lib.sdm_decode_seq_ex.argtypes = dec + [i32, i32, i32, ctypes.c_uint, vp]
+            lib.sdm_decode_seq_ex.restype = i32
             lib.sdm_gather.argtypes = [vp, i64, i32, i32, i32, ctypes.POINTER(vp), ctypes.POINTER(vp),
                                        ctypes.POINTER(vp), ctypes.POINTER(i32), i32, i32, vp, i64, i32, i32, vp, vp]
             lib.sdm_gather.restype = i32
@@ -166,13 +170,25 @@ def decode_step(bank, k_idx, k_val, v, beta, g, q_idx, q_val, out=None, stream=N
     return out
 
 
-def decode_seq(bank, k_idx, k_val, v, beta, g, q_idx, q_val, out=None, stream=None) -> torch.Tensor:
+def decode_seq(bank, k_idx, k_val, v, beta, g, q_idx, q_val, out=None, stream=None, *, stream_major: bool = False,
+               inputs_ready: bool = False) -> torch.Tensor:
     """T tokens for every stream in one launch (sdm_decode_seq). Arrays are time-major [T, S, .],
-    beta is [T, S]; returns the readings [T, S, hd]."""
-    T, S = k_idx.shape[0], k_idx.shape[1]
-    out, ptrs, hd, W, R, G, st = _decode_args(bank, k_idx, k_val, v, beta, g, q_idx, q_val, out, (T, S), stream)
-    rc = library().sdm_decode_seq(*ptrs, S, hd, W, R, G, T, _BANK_CODES[bank.dtype], _IDX_CODES[k_idx.dtype], st)
-    _check("sdm_decode_seq", rc)
+    beta is [T, S]; returns the readings [T, S, hd].
+
+    ``stream_major`` (sdm_decode_seq_ex with SDM_STREAM_MAJOR): the arrays are in the layer's own
+    prompt layout [S, T, .] (beta [S, T]) and the readings come back as [S, T, hd]; no staging copy
+    is made. ``inputs_ready``: SDM_INPUTS_READY, as for decode_step."""
+    lead = tuple(k_idx.shape[:2])
+    S, T = lead if stream_major else lead[::-1]
+    out, ptrs, hd, W, R, G, st = _decode_args(bank, k_idx, k_val, v, beta, g, q_idx, q_val, out, lead, stream)
+    codes = (_BANK_CODES[bank.dtype], _IDX_CODES[k_idx.dtype])
+    flags = (SDM_STREAM_MAJOR if stream_major else 0) | (SDM_INPUTS_READY if inputs_ready else 0)
+    if flags:
+        rc = library().sdm_decode_seq_ex(*ptrs, S, hd, W, R, G, T, *codes, flags, st)
+        _check("sdm_decode_seq_ex", rc)
+    else:
+        rc = library().sdm_decode_seq(*ptrs, S, hd, W, R, G, T, *codes, st)
+        _check("sdm_decode_seq", rc)
     return out
 
 

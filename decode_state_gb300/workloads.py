@@ -90,7 +90,14 @@ C4 = GatherWorkload("gather_bf16_4M_hd128_65536tok_2x64_stash", "bf16", 4194304,
 C4_BWD = GatherWorkload("gather_bwd_f32_4M_hd128_65536tok_1x64_stash", "f32", 4194304, 128, 65536, 64, (64,), "i64",
                         "f32", 1 / 8)
 
-DECODE_WORKLOADS = {w.name: w for w in (C0, C1, C2, C3)}
+# A prompt run through the recurrent form: the serving geometry per stream (bf16, hd 128,
+# W = R = 64, one gate per token, 16384 slots each) for 64 streams of 1024 tokens, with every
+# per-token array in the layer's own stream-major layout [S, T, .] (the benchmark transposes the
+# time-major draw once, before timing).
+PROMPT = DecodeWorkload("prompt_bf16_s64_hd128_w64_t1024_stream_major", "bf16", 64, 128, 16384, 64, 64, 1, 1024,
+                        "i32", 1 / math.sqrt(8), mode="seq_stream_major")
+
+DECODE_WORKLOADS = {w.name: w for w in (C0, C1, C2, C3, PROMPT)}
 GATHER_WORKLOADS = {w.name: w for w in (C4, C4_BWD)}
 
 

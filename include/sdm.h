@@ -3,7 +3,8 @@
  *
  * Three operations, each one kernel launch on the caller's stream:
  *   sdm_decode_step  one write-then-read token for every stream (sdm_decode_step_ex: with flags)
- *   sdm_decode_seq   T tokens for every stream in one persistent launch
+ *   sdm_decode_seq   T tokens for every stream in one persistent launch (sdm_decode_seq_ex: with
+ *                    flags, e.g. the stream-major [n_streams, T, .] layout of a prompt)
  *   sdm_gather       per-token weighted sums of bank rows (one or two operands), optional stash
  *                    (sdm_gather_kpos: with a compact snapshot instead; sdm_gather_plan_*: a
  *                    checked launch, replayed per slab of an index tensor; _launch_ex: with
@@ -135,6 +136,24 @@ int sdm_decode_step_ex(void* bank, const void* k_idx, const float* k_val, const 
 int sdm_decode_seq(void* bank, const void* k_idx, const float* k_val, const float* v, const float* beta,
                    const float* g, const void* q_idx, const float* q_val, void* out, int64_t n_streams, int hd,
                    int W, int R, int G, int T, int bank_dtype, int idx_dtype, sdm_stream_t stream);
+
+/*
+ * sdm_decode_seq_ex - sdm_decode_seq with flags; flags == 0 is sdm_decode_seq.
+ *
+ * SDM_STREAM_MAJOR: every per-token array is in the layer's own stream-major layout, each
+ * stream's T tokens contiguous: k_idx, k_val [n_streams, T, W]; v [n_streams, T, hd]; beta
+ * [n_streams, T]; g [n_streams, T, G]; q_idx, q_val [n_streams, T, R]; and the readings go to
+ * out [n_streams, T, hd]. This is the [P, T, .] layout of a prompt that forward_steps
+ * (forward.py) stages to time-major with stage_time_major before its steps and whose readings it
+ * takes back with unstage_time_major; here the kernel reads and writes that layout by stride, so
+ * neither staging copy is made. Results are the bits of sdm_decode_seq on the staged arrays.
+ * SDM_INPUTS_READY: as for sdm_decode_step_ex (token 0's inputs are read before the wait).
+ * Unknown bits return SDM_EFLAGS. Other arguments as sdm_decode_seq.
+ */
+#define SDM_STREAM_MAJOR 2u
+int sdm_decode_seq_ex(void* bank, const void* k_idx, const float* k_val, const float* v, const float* beta,
+                      const float* g, const void* q_idx, const float* q_val, void* out, int64_t n_streams, int hd,
+                      int W, int R, int G, int T, int bank_dtype, int idx_dtype, unsigned flags, sdm_stream_t stream);
 
 /*
  * sdm_gather - token gather (gather_cuda.py, module docstring and token_gather).

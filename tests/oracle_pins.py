@@ -308,6 +308,60 @@ def pin_decay_only(orc):
                 assert_bits_equal(bank[slot], to_bank(ref, dtype), f"{dtype} decay of slot {slot}")
 
 
+_WIDE_GATES = {}
+
+
+def f32_from_decimal(val: decimal.Decimal) -> np.float32:
+    """The float32 nearest to a positive Decimal in the float32 normal range: through the nearest
+    double, except when that double lies exactly on a float32 rounding midpoint, where the double
+    rounding could go the wrong way and the exact rational rounding decides."""
+    x = float(val)
+    bits = int(np.array([x], dtype=np.float64).view(np.uint64)[0])
+    if bits & ((1 << 29) - 1) == 1 << 28:  # the 29 bits below a float32 mantissa: exactly one half
+        return f32_nearest(fractions.Fraction(val))
+    return np.float32(x)
+
+
+def wide_gates():
+    """About 10^5 float32 gates and the float32 nearest to e^g of each (decimal's exp at 34 digits,
+    correctly rounded), computed once per process: the workload's distribution -softplus(N(0,1)),
+    uniform values over [-87, 88], and magnitudes log-uniform over [2^-30, 2^6] of both signs."""
+    if "g" not in _WIDE_GATES:
+        rng = np.random.default_rng(2024)
+        g = np.concatenate([
+            -np.log1p(np.exp(rng.normal(size=60000))),
+            rng.uniform(-87.0, 88.0, size=25000),
+            rng.choice([-1.0, 1.0], size=15000) * np.exp2(rng.uniform(-30.0, 6.0, size=15000)),
+        ]).astype(np.float32)
+        g = g[(g >= -87.0) & (g <= 88.0)]
+        ctx = decimal.Context(prec=34)
+        d = np.array([f32_from_decimal(ctx.exp(decimal.Decimal(float(x)))) for x in g], dtype=np.float32)
+        _WIDE_GATES["g"], _WIDE_GATES["d"] = g, d
+    return _WIDE_GATES["g"], _WIDE_GATES["d"]
+
+
+def pin_gates_nearest_exp(orc):
+    """Every gate d = exp(g) is the float32 nearest to e^g, over about 10^5 gates. Each gate is read
+    back through the write: a float32 bank of ones, beta = 0 and k_val = 0 make every written row
+    1 * d_w = d_w exactly (G = W, 256 writes per token, fresh slots every token)."""
+    g_all, d_ref = wide_gates()
+    W = 256
+    T = (len(g_all) + W - 1) // W
+    n = T * W
+    g = np.resize(g_all, n).reshape(T, 1, W)
+    f = np.float32
+    bank = np.ones((n, 1), dtype=f)
+    case = dict(k_idx=np.arange(n, dtype=np.int64).reshape(T, 1, W), k_val=np.zeros((T, 1, W), f),
+                v=np.zeros((T, 1, 1), f), beta=np.zeros((T, 1), f), g=g.astype(f),
+                q_idx=np.zeros((T, 1, 1), np.int64), q_val=np.zeros((T, 1, 1), f))
+    orc.decode_seq(bank, case["k_idx"], case["k_val"], case["v"], case["beta"], case["g"], case["q_idx"],
+                   case["q_val"])
+    got = bank[:len(g_all), 0]
+    bad = np.flatnonzero(got.view(np.uint32) != d_ref.view(np.uint32))
+    assert bad.size == 0, (f"{bad.size} of {len(g_all)} gates are not the float32 nearest to e^g; first g = "
+                           f"{float(g_all[bad[0]]).hex()}: {got[bad[0]]!r} vs {d_ref[bad[0]]!r}")
+
+
 def pin_gate_sharing(orc):
     """G=1 and G=W with every per-write gate equal to the shared gate give identical bits."""
     rng = np.random.default_rng(6)

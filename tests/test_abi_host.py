@@ -85,6 +85,19 @@ def test_decode_step_ex_flags(lib):
     assert lib.sdm_decode_step_ex(*args[:9], 0, *args[10:], sdm.SDM_INPUTS_READY, None) == 0  # no streams
 
 
+def test_decode_seq_ex_flags(lib):
+    """Unknown flag bits are refused first; the stream-major layout and the inputs-ready promise
+    validate like sdm_decode_seq."""
+    args = (FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4, 64, 8, 8, 1, 3, 0, 0)
+    assert lib.sdm_decode_seq_ex(*args, 4, None) == CODES["SDM_EFLAGS"]
+    assert lib.sdm_decode_seq_ex(*args, sdm.SDM_STREAM_MAJOR | 8, None) == CODES["SDM_EFLAGS"]
+    bad = args[:11] + (257,) + args[12:]
+    for flags in (0, sdm.SDM_STREAM_MAJOR, sdm.SDM_INPUTS_READY, sdm.SDM_STREAM_MAJOR | sdm.SDM_INPUTS_READY):
+        assert lib.sdm_decode_seq_ex(*bad, flags, None) == CODES["SDM_EWIDTH"]
+        assert lib.sdm_decode_seq_ex(*args[:9], 0, *args[10:], flags, None) == 0  # no streams
+        assert lib.sdm_decode_seq_ex(*args[:14], 0, *args[15:], flags, None) == 0  # no tokens
+
+
 def test_decode_step_validates_like_seq(lib):
     assert lib.sdm_decode_step(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4, 64, 0, 8, 1, 0, 0,
                                None) == CODES["SDM_EWIDTH"]

@@ -145,9 +145,10 @@ def test_device_status_waits_for_side_streams():
 @pytest.mark.parametrize("wl", [workloads.C4, workloads.C4_BWD], ids=lambda w: w.name)
 def test_gather_full_size(wl):
     """A full gather workload in the benchmark's launch configuration (the two-operand forward
-    shape and the one-operand backward shape): sampled tokens against the oracle bit for bit,
-    every stash row against torch's own row indexing, every padding token zero, and every output
-    within the float32 summation bound of a float64 evaluation."""
+    shape and the one-operand backward shape): every token's outputs and stash rows against the
+    oracle run over the whole launch, bit for bit; every stash row also against torch's own row
+    indexing, every padding token zero, and every output within the float32 summation bound of a
+    float64 evaluation."""
     g = workloads.make_gather_inputs(wl, device=DEV)
     outs, stash = sdm.gather(g["bank"], g["ops"], chunk=wl.chunk, chunk_valid=g["chunk_valid"])
     torch.cuda.synchronize()
@@ -167,12 +168,11 @@ def test_gather_full_size(wl):
         ref = torch.einsum("tn,tnc->tc", wd, rows)
         bound = idx.shape[1] * 2.0 ** -24 * torch.einsum("tn,tnc->tc", wd.abs(), rows.abs()) * 1.01
         assert bool(((out[live].double() - ref).abs() <= bound).all())
-    # sampled tokens against the oracle, bit for bit
-    bank_h = to_np(g["bank"])
-    sample = torch.nonzero(live).flatten()[:: max(1, int(live.sum()) // 256)][:256]
-    for o, (idx, w) in enumerate(g["ops"]):
-        ref, _, _ = oracle.gather(bank_h, to_np(idx[sample]), to_np(w[sample]), chunk=1, stash=False)
-        assert bits_equal(to_np(outs[o][sample]), ref)
+    # the whole launch against the oracle, bit for bit
+    ref = _oracle(g, wl)
+    for o in range(len(g["ops"])):
+        assert bits_equal(to_np(outs[o]), ref[o]), f"operand {o} outputs differ from the oracle"
+    assert bits_equal(to_np(stash), ref[2]), "stash differs from the oracle"
 
 
 def _first_occurrence_kpos(idx: np.ndarray, chunk: int, live: np.ndarray) -> np.ndarray:
@@ -269,3 +269,15 @@ def test_gather_kpos_full_size():
     for a, b in zip(outs, outs_ref):
         assert torch.equal(a.view(torch.int32), b.view(torch.int32))
     assert sdm.device_status() == 0
+    # the whole launch against the oracle, bit for bit: the snapshot (sentinel rows included) and
+    # both operands' outputs
+    bank_h = to_np(g["bank"])
+    ref_compact = np.full(compact.shape, to_np(sentinel)[0], dtype=np.uint16)
+    oracle.gather_kpos(bank_h, to_np(idx0), to_np(kpos), ref_compact, chunk=wl.chunk,
+                       chunk_valid=to_np(g["chunk_valid"]), check=False)
+    assert bits_equal(to_np(compact), ref_compact), "compact snapshot differs from the oracle"
+    del ref_compact
+    (i0, w0), (i1, w1) = g["ops"]
+    r0, r1, _ = oracle.gather(bank_h, to_np(i0), to_np(w0), to_np(i1), to_np(w1), chunk=wl.chunk,
+                              chunk_valid=to_np(g["chunk_valid"]), stash=False, check=False)
+    assert bits_equal(to_np(outs[0]), r0) and bits_equal(to_np(outs[1]), r1), "outputs differ from the oracle"

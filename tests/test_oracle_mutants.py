@@ -21,6 +21,8 @@ MUTANTS = {
     "q_val_unrounded": ("float qv = round_to_bank(q_val[s * R + r], bank_dtype);", "float qv = q_val[s * R + r];"),
     "v_unrounded": ("float vr = round_to_bank(v[s * hd + c], bank_dtype);", "float vr = v[s * hd + c];"),
     "shared_gate_index": ("g[s * G + (G == 1 ? 0 : w)]", "g[s * G]"),
+    "gate_single_precision_exp": ("d[w] = (float)exp((double)g[s * G + (G == 1 ? 0 : w)]);",
+                                  "d[w] = expf(g[s * G + (G == 1 ? 0 : w)]);"),
     "bf16_round_half_up": ("u += 0x7fffu + ((u >> 16) & 1u);", "u += 0x8000u;"),
     "seq_reuses_token0": ("const char* kit = (const char*)k_idx + (size_t)(t * n_streams * W) * ies;",
                           "const char* kit = (const char*)k_idx;"),
