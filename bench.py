@@ -228,15 +228,17 @@ def oracle_gather_tokens(bank_h, g: dict, tokens, chunk: int):
 
 
 def decode_config(wl, r: sdist.Rank, call: str) -> dict:
-    """The config object of a decode workload's JSON line; both arms use it, so that they name the
-    same workload with the same keys (only `call` differs)."""
+    """The config object of a decode workload's JSON line (wl: one rank's share); both arms use
+    it, so that they name the same workload with the same keys (only `call` differs)."""
     bank_gib = wl.n_slots * wl.hd * (2 if wl.bank_dtype == "bf16" else 4) / 2 ** 30
     return {"workload": wl.name, "streams": wl.n_streams, "head_dim": wl.hd,
             "slots_per_stream": wl.slots_per_stream, "W": wl.W, "R": wl.R, "G": wl.G, "T": wl.T,
             "bank_dtype": wl.bank_dtype, "idx_dtype": wl.idx_dtype, "call": call,
             "l2": (f"inputs larger than L2 ({bank_gib:.2f} GiB bank), no flush" if bank_gib > 0.2 else
                    f"L2-resident ({bank_gib * 1024:.0f} MiB bank)"),
-            "parallelism": f"weak: {r.world} independent shard(s), no collective in the data path"}
+            "parallelism": (f"weak: a job of {wl.n_streams * r.world} streams split into {r.world} contiguous "
+                            f"stream range(s) of {wl.n_streams}, each rank holding its streams' bank rows; no "
+                            f"collective in the data path")}
 
 
 class Case:
@@ -255,7 +257,13 @@ class Case:
             if args.tokens:
                 wl = wl.scaled(T=args.tokens)
             self.kind = "decode_" + wl.mode
-            self.x = workloads.make_decode_inputs(wl, device=dev, seed=sdist.shard_seed(wl.seed, r))
+            # weak scaling: the job holds wl.n_streams streams per rank, split into contiguous
+            # stream ranges; this rank draws only its own streams and their bank rows
+            job = wl.scaled(n_streams=wl.n_streams * r.world)
+            lo, hi = sdist.stream_shard(job.n_streams, r, workloads.SHARD_BLOCK)
+            self.x = workloads.make_decode_shard(job, lo, hi, device=dev)
+            self.shard = (lo, hi, job.n_streams)
+            wl = wl.scaled(n_streams=hi - lo)
             bdt = workloads.BANK_DTYPES[wl.bank_dtype]
             self.out = torch.empty((wl.T, wl.n_streams, wl.hd), dtype=bdt, device=dev)
             if self.kind == "decode_seq_stream_major":  # the prompt's own layout [S, T, .], made once
@@ -265,7 +273,9 @@ class Case:
             self.unit = UNIT
             self.launches = 1 if wl.mode.startswith("seq") else wl.T
             self.nbytes = workloads.decode_bytes_per_stream_token(wl) * wl.n_streams * wl.T
-            self.kernel = f"decode_vec_kernel<{wl.bank_dtype},{wl.idx_dtype}>"
+            # float32 rows that cannot all be staged stream through a ring (decode_wide_kernel)
+            wide = wl.bank_dtype == "f32" and max(wl.W, wl.R) * min(wl.hd, 256) * 4 > 32768
+            self.kernel = f"{'decode_wide_kernel' if wide else 'decode_vec_kernel'}<{wl.bank_dtype},{wl.idx_dtype}>"
             self.metric = METRIC
         else:
             wl = workloads.GATHER_WORKLOADS[name]
@@ -300,7 +310,7 @@ class Case:
 
     def config(self, r: sdist.Rank) -> dict:
         wl = self.wl
-        par = f"weak: {r.world} independent shard(s), no collective in the data path"
+        par = f"weak: {r.world} independent token shard(s), bank drawn per rank, no collective in the data path"
         if self.kind == "gather":
             gib = wl.n_slots * wl.hd * (2 if wl.bank_dtype == "bf16" else 4) / 2 ** 30
             return {"workload": wl.name, "n_slots": wl.n_slots, "head_dim": wl.hd, "tokens": wl.tokens,
@@ -674,13 +684,16 @@ def kpos_gather(dev, peak: float) -> dict:
 
 def run_reference(args, r: sdist.Rank):
     """The CPU oracle on the host cores: each step is the oracle over a bounded sample of whole
-    streams of the same workload (drawn on the host with the same generator recipe)."""
+    streams of the same workload: the first streams of the benchmark's own job (its first block of
+    streams, drawn on the host with the same recipe and seed)."""
     if args.workload not in workloads.DECODE_WORKLOADS:
         raise SystemExit("--impl reference times the decode workloads")
     base = workloads.DECODE_WORKLOADS[args.workload]
     n_pool = min(8, base.n_streams)
     wl = base.scaled(n_streams=n_pool)
-    x = workloads.make_decode_inputs(wl, device="cpu", seed=base.seed)
+    xb = workloads.make_decode_shard(base, 0, min(workloads.SHARD_BLOCK, base.n_streams), device="cpu")
+    x = {k: (v[:, :n_pool] if k in DECODE_KEYS else v[:n_pool * base.slots_per_stream]) for k, v in xb.items()}
+    del xb
     _, per_stream_s = oracle_stream_tokens(x, [0], wl.slots_per_stream)
     total = args.steps + args.warmup
     budget = 90.0
@@ -701,8 +714,8 @@ def run_reference(args, r: sdist.Rank):
         done += step(i)[0]
     secs = time.perf_counter() - t0
     value = done / secs
-    sample = (f"{per_step_streams} whole stream(s) x {T_used} token(s) per step, cycling over {n_pool} streams "
-              f"drawn with the workload's recipe")
+    sample = (f"{per_step_streams} whole stream(s) x {T_used} token(s) per step, cycling over the first {n_pool} "
+              f"streams of the benchmark's own job")
     return {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": r.world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs * 1e3 / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",

@@ -240,9 +240,8 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
 // Every thread: cp.async copies of token ts's slots, weights, gates and beta into the raw area.
-template <typename I>
-__device__ __forceinline__ void prefetch_meta(const DecodeArgs& a, int64_t ts, const VecLayout& L,
-                                              unsigned char* smem) {
+template <typename I, typename Layout>
+__device__ __forceinline__ void prefetch_meta(const DecodeArgs& a, int64_t ts, const Layout& L, unsigned char* smem) {
     const int tid = threadIdx.x, nt = blockDim.x, W = a.W, R = a.R, G = a.G;
     I* rk = reinterpret_cast<I*>(smem + L.raw_k);
     I* rq = reinterpret_cast<I*>(smem + L.raw_q);
@@ -330,6 +329,9 @@ __device__ __forceinline__ void ldgsts_rows(E* rows, const unsigned char* bank, 
     cp_async_commit();
 }
 
+// an L2 prefetch (a hint: nothing reaches the SM) of the 128-byte line at p
+__device__ __forceinline__ void pf_l2(const void* p) { asm volatile("prefetch.global.L2 [%0];" ::"l"(p)); }
+
 // L2 prefetches (hints: nothing reaches the SM) of the 128-byte lines of n row slices bank + off[r]
 __device__ __forceinline__ void prefetch_rows_l2(const unsigned char* bank, const int64_t* off, int n,
                                                  uint32_t row_bytes) {
@@ -408,7 +410,7 @@ __global__ void __launch_bounds__(kMaxThreads, 2) decode_vec_kernel(const Decode
             const int lines = (int)((row_bytes + 127) >> 7);
             for (int i = tid; i < R * lines; i += blockDim.x) {
                 const int r = i / lines, l = i - r * lines;
-                asm volatile("prefetch.global.L2 [%0];" ::"l"(bank + qoff[r] + (int64_t)l * 128));
+                pf_l2(bank + qoff[r] + (int64_t)l * 128);
             }
         }
         uint64_t vr = 0;
@@ -518,7 +520,7 @@ __global__ void __launch_bounds__(kMaxThreads, 2) decode_vec_kernel(const Decode
             for (int i = tid; i < W * lines; i += blockDim.x) {
                 const int r = i / lines, l = i - r * lines;
                 const unsigned char* p = bank + (int64_t)rk[r] * rowb + colb + (int64_t)l * 128;
-                asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+                pf_l2(p);
             }
         }
         cp_async_wait_all();
@@ -642,7 +644,7 @@ __global__ void __launch_bounds__(128, 7) decode_vec1_kernel(const DecodeArgs a,
             const int lines = (int)((row_bytes + 127) >> 7);
             for (int i = tid; i < R * lines; i += nt) {
                 const int r = i / lines, l = i - r * lines;
-                asm volatile("prefetch.global.L2 [%0];" ::"l"(bank + qoff[r] + (int64_t)l * 128));
+                pf_l2(bank + qoff[r] + (int64_t)l * 128);
             }
         }
         const float vr = active ? round_to<E>(__ldg(a.v + ts * hd + c0 + j)) : 0.0f;
@@ -718,7 +720,7 @@ __global__ void __launch_bounds__(128, 7) decode_vec1_kernel(const DecodeArgs a,
             for (int i = tid; i < W * lines; i += nt) {
                 const int r = i / lines, l = i - r * lines;
                 const unsigned char* p = bank + (int64_t)rk[r] * rowb + colb + (int64_t)l * 128;
-                asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+                pf_l2(p);
             }
         }
         cp_async_wait_all();
@@ -927,136 +929,316 @@ __global__ void __launch_bounds__(kMaxThreads, 1) decode_stream_kernel(const Dec
     }
 }
 
-// The streaming path for float32 banks with one column per thread, for slices of up to 128
-// columns: the same ring, metadata and order of operations as decode_stream_kernel, but scalar
-// float32 chains (each lane of a paired op is an independent round-to-nearest op, so the bits are
-// the same) and twice the warps to cover the chains' latency.
+// ---------------------------------------------------------------- streaming path, float32, a column per thread
+//
+// Float32 banks whose W or R rows cannot all be staged (e.g. 256 rows of 1 KiB) stream their row
+// slices through a ring of NS chunks of CH rows, one column per thread, slices of up to 256
+// columns chosen at launch so that the grid balances over the SMs (e.g. 256 streams of 1 KiB rows:
+// 1024 quarter-row blocks, 7 per SM). The block's metadata is kept lean so that the ring stays
+// deep at that occupancy: byte offsets of the rows and single float weights.
+//
+// Each block runs one job list per "segment": the read chunks of token t-1, then the retrieve
+// chunks and the decay-and-write chunks of token t (the write rows pass twice: retrieve, then
+// write; the second pass is served by L2). The ring runs through a segment without draining: the
+// read rows of token t-1 and the write rows of token t are both read after token t-1's writes and
+// before token t's, so their copies can run back to back. It drains only at the end of a segment,
+// where token t's writes must be complete before token t's read rows are copied. A chunk's stage
+// is refilled as soon as every thread has consumed it, before the next chunk is awaited, so that
+// all NS stages are in flight during each wait.
+// Chunks are consumed in ascending row order, so every sum keeps the staged path's order and bits.
+
+struct WideLayout {
+    size_t koff, kv, dw, beta, qoff, qv, ring, total;
+    __host__ __device__ WideLayout(int W, int R, int G, int sw, int ch, int ns) {
+        koff = 0;  // the write side (copied in place, then turned into offsets and gates)
+        kv = align_up(koff + (size_t)W * 8, 16);
+        dw = align_up(kv + (size_t)W * 4, 16);
+        beta = align_up(dw + (size_t)G * 4, 16);
+        qoff = align_up(beta + 4, 16);  // the read side (copied in place, then turned into offsets)
+        qv = align_up(qoff + (size_t)R * 8, 16);
+        ring = align_up(qv + (size_t)R * 4, 128);
+        total = ring + (size_t)ns * ch * sw * 4;
+    }
+};
+
+// Every thread: cp.async copies of token ts's write-side inputs in place: the slots into the offset
+// array (64-bit slots one per entry; 32-bit slots into its upper half), the weights into kv, the
+// log-decays into dw, beta (no commit). wide_derive_k turns slots into row offsets, log-decays into
+// gates.
+template <typename I>
+__device__ __forceinline__ void wide_load_k(const DecodeArgs& a, int64_t ts, const WideLayout& L, unsigned char* smem) {
+    const int tid = threadIdx.x, nt = blockDim.x, W = a.W, G = a.G;
+    I* rk = reinterpret_cast<I*>(smem + L.koff + (sizeof(I) == 8 ? 0 : (size_t)W * 4));
+    float* kv = reinterpret_cast<float*>(smem + L.kv);
+    float* dw = reinterpret_cast<float*>(smem + L.dw);
+    const I* k_idx = static_cast<const I*>(a.k_idx) + ts * W;
+    for (int i = tid; i < W; i += nt) {
+        if constexpr (sizeof(I) == 8)
+            cp_async8(rk + i, k_idx + i);
+        else
+            cp_async4(rk + i, k_idx + i);
+        cp_async4(kv + i, a.k_val + ts * W + i);
+    }
+    for (int i = tid; i < G; i += nt) cp_async4(dw + i, a.g + ts * G + i);
+    if (tid == 0) cp_async4(smem + L.beta, a.beta + ts);
+}
+
+// Every thread: cp.async copies of token ts's read-side inputs in place: the slots into the offset
+// array (64-bit slots one per entry; 32-bit slots into its upper half), the weights into qv (no
+// commit). wide_derive_q turns them into row offsets.
+template <typename I>
+__device__ __forceinline__ void wide_load_q(const DecodeArgs& a, int64_t ts, const WideLayout& L, unsigned char* smem) {
+    const int tid = threadIdx.x, nt = blockDim.x, R = a.R;
+    I* rq = reinterpret_cast<I*>(smem + L.qoff + (sizeof(I) == 8 ? 0 : (size_t)R * 4));
+    float* qv = reinterpret_cast<float*>(smem + L.qv);
+    const I* q_idx = static_cast<const I*>(a.q_idx) + ts * R;
+    for (int i = tid; i < R; i += nt) {
+        if constexpr (sizeof(I) == 8)
+            cp_async8(rq + i, q_idx + i);
+        else
+            cp_async4(rq + i, q_idx + i);
+        cp_async4(qv + i, a.q_val + ts * R + i);
+    }
+}
+
+// Every thread: the write side copied in place becomes row byte offsets and gates d = exp(g) (the
+// weights are used as given; a = kv * d is formed where it is used). 32-bit slots sit in the upper
+// half of the offset array, which the offsets overwrite, and a shared gate is read by every thread
+// and then replaced by one: so every thread reads first (at most 256 / 32 slots) and writes after a
+// barrier.
+template <typename I>
+__device__ __forceinline__ void wide_derive_k(const DecodeArgs& a, int c0, const WideLayout& L, unsigned char* smem) {
+    const int tid = threadIdx.x, nt = blockDim.x, W = a.W, G = a.G;
+    const int64_t rowb = (int64_t)a.hd * 4, colb = (int64_t)c0 * 4;
+    int64_t* koff = reinterpret_cast<int64_t*>(smem + L.koff);
+    float* dw = reinterpret_cast<float*>(smem + L.dw);
+    const I* rk = reinterpret_cast<const I*>(smem + L.koff + (sizeof(I) == 8 ? 0 : (size_t)W * 4));
+    int64_t k[kMaxThreads / 32];
+#pragma unroll
+    for (int u = 0; u < kMaxThreads / 32; ++u) k[u] = tid + u * nt < W ? (int64_t)rk[tid + u * nt] : 0;
+    const float g1 = dw[0];
+    __syncthreads();
+#pragma unroll
+    for (int u = 0; u < kMaxThreads / 32; ++u) {
+        const int i = tid + u * nt;
+        if (i < W) {
+            koff[i] = k[u] * rowb + colb;
+            if (G != 1) dw[i] = gate(dw[i]);
+        }
+    }
+    if (G == 1 && tid == 0) dw[0] = gate(g1);
+}
+
+// Every thread: the read-side slots copied in place become row byte offsets (the weights are used as
+// given). 32-bit slots sit in the upper half of the offset array, which the offsets overwrite: every
+// thread reads its slots first (at most 256 / 32 per thread), and writes after a barrier.
+template <typename I>
+__device__ __forceinline__ void wide_derive_q(const DecodeArgs& a, int c0, const WideLayout& L, unsigned char* smem) {
+    const int tid = threadIdx.x, nt = blockDim.x, R = a.R;
+    const int64_t rowb = (int64_t)a.hd * 4, colb = (int64_t)c0 * 4;
+    int64_t* qoff = reinterpret_cast<int64_t*>(smem + L.qoff);
+    if constexpr (sizeof(I) == 8) {
+        for (int i = tid; i < R; i += nt) qoff[i] = qoff[i] * rowb + colb;
+    } else {
+        const int* rq = reinterpret_cast<const int*>(smem + L.qoff + (size_t)R * 4);
+        int q[kMaxThreads / 32];
+#pragma unroll
+        for (int u = 0; u < kMaxThreads / 32; ++u) q[u] = tid + u * nt < R ? rq[tid + u * nt] : 0;
+        __syncthreads();
+#pragma unroll
+        for (int u = 0; u < kMaxThreads / 32; ++u) {
+            const int i = tid + u * nt;
+            if (i < R) qoff[i] = (int64_t)q[u] * rowb + colb;
+        }
+    }
+}
+
+constexpr int kWideRegs = 128;  // registers per thread of decode_wide_kernel, at most (2 blocks of 256)
+
 template <typename I, int NS>
-__global__ void __launch_bounds__(kMaxThreads, 1) decode_stream1_kernel(const DecodeArgs a, int early_trigger) {
-    constexpr int ES = 4;
+__global__ void __launch_bounds__(kMaxThreads, 65536 / (kMaxThreads * kWideRegs))
+    decode_wide_kernel(const DecodeArgs a, int early_trigger) {
     const int CH = a.stream_rows;
     extern __shared__ __align__(128) unsigned char smem[];
 
-    const int W = a.W, R = a.R, G = a.G, hd = a.hd, sw = a.slice_cols;
-    const StreamLayout SL(W, R, G, sw, ES, (int)sizeof(I), CH, NS);
-    const VecLayout& L = SL.meta;
-    unsigned char* ring = smem + SL.ring;
-    const size_t stage_bytes = (size_t)CH * sw * ES;
+    const int W = a.W, R = a.R, G = a.G, hd = a.hd, sw = a.slice_cols, T = a.T;
+    const WideLayout L(W, R, G, sw, CH, NS);
+    unsigned char* ring = smem + L.ring;
+    const size_t stage_bytes = (size_t)CH * sw * 4;
     const int64_t* koff = reinterpret_cast<const int64_t*>(smem + L.koff);
     const int64_t* qoff = reinterpret_cast<const int64_t*>(smem + L.qoff);
-    const uint64_t* aw2 = reinterpret_cast<const uint64_t*>(smem + L.aw2);
-    const uint64_t* kv2 = reinterpret_cast<const uint64_t*>(smem + L.kv2);
-    const uint64_t* dw2 = reinterpret_cast<const uint64_t*>(smem + L.dw2);
-    const uint64_t* qv2 = reinterpret_cast<const uint64_t*>(smem + L.qv2);
+    const float* kv = reinterpret_cast<const float*>(smem + L.kv);
+    const float* dw = reinterpret_cast<const float*>(smem + L.dw);
+    const float* qv = reinterpret_cast<const float*>(smem + L.qv);
 
-    const int tid = threadIdx.x;
+    const int tid = threadIdx.x;  // this thread's column within the slice
+    unsigned char* bank = static_cast<unsigned char*>(a.bank);
+    float* out = static_cast<float*>(a.out);
+    const int64_t jb = (int64_t)tid * 4;
+    const int nk = (W + CH - 1) / CH, nq = (R + CH - 1) / CH;
     const int64_t s = blockIdx.x / a.n_slices;
     const int c0 = (int)(blockIdx.x % a.n_slices) * sw;
     const int ncols = min(sw, hd - c0);
-    const int j = tid;
-    const bool active = j < ncols;
-    const uint32_t row_bytes = (uint32_t)ncols * ES;
-    unsigned char* bank = static_cast<unsigned char*>(a.bank);
-    float* out = static_cast<float*>(a.out);
-    const int64_t jb = (int64_t)j * ES;
-    const int nk = (W + CH - 1) / CH, nq = (R + CH - 1) / CH;
-    const auto at = [&](int st, int r) -> float {
-        return reinterpret_cast<const float*>(ring + st * stage_bytes)[r * sw + tid];
-    };
+    const bool active = tid < ncols;
+    const uint32_t row_bytes = (uint32_t)ncols * 4;
 
-    if (!a.inputs_ready) {  // as in decode_stream_kernel
+    // With inputs_ready the inputs predate the preceding kernel: token 0's write side is read and its
+    // rows are warmed in L2 before waiting for that kernel; the bank is read and written (and `out`
+    // written) only after the wait.
+    if (!a.inputs_ready) {
         grid_dependency_wait();
         if (early_trigger) grid_launch_dependents();
     }
-    prefetch_meta<I>(a, s * a.sstride, L, smem);  // token 0
+    const int64_t ts0 = s * a.sstride;  // token 0 of this stream
+    wide_load_k<I>(a, ts0, L, smem);
+    cp_async_commit();
     cp_async_wait_all();
     __syncthreads();
-    if (G == 1 && tid == 0)
-        *reinterpret_cast<float*>(smem + L.dnext) = gate(*reinterpret_cast<const float*>(smem + L.raw_g));
+    wide_derive_k<I>(a, c0, L, smem);
     __syncthreads();
-    derive_meta<float, I>(a, c0, L, smem);
-    __syncthreads();
+    // the write side of a later token is copied at the start of its segment and derived before its
+    // first write-row copy, which the ring issues NS - 1 jobs ahead: at job nq - NS + 1
+    const int kd = nq - NS + 1;
     if (a.inputs_ready) {
         prefetch_rows_l2(bank, koff, W, row_bytes);
-        prefetch_rows_l2(bank, qoff, R, row_bytes);
         grid_dependency_wait();
         if (early_trigger) grid_launch_dependents();
     }
 
-    for (int t = 0; t < a.T; ++t) {
-        const int64_t ts = (int64_t)t * a.tstride + s * a.sstride;
-        const float vr = active ? __ldg(a.v + ts * hd + c0 + j) : 0.0f;
-        const float beta = *reinterpret_cast<const float*>(smem + L.beta);
-        const float dsh = f2lo(dw2[0]);
-
-        float acc = 0.0f, delta = 0.0f;
-        const int jobs = 2 * nk;
-        for (int q = 0; q < NS - 1; ++q) {
-            if (q < jobs) {
-                const int c = q % nk;
-                ldgsts_chunk<float>(ring + (q % NS) * stage_bytes, bank, koff, c * CH, min(CH, W - c * CH), sw, row_bytes);
-            } else {
-                cp_async_commit();
-            }
-        }
-        for (int q = 0; q < jobs; ++q) {
-            const int qn = q + NS - 1;
-            if (qn < jobs) {
-                const int c = qn % nk;
-                ldgsts_chunk<float>(ring + (qn % NS) * stage_bytes, bank, koff, c * CH, min(CH, W - c * CH), sw, row_bytes);
-            } else {
-                cp_async_commit();
-            }
-            asm volatile("cp.async.wait_group %0;" ::"n"(NS - 1) : "memory");
+    float racc = 0.0f, acc = 0.0f, delta = 0.0f, vr = 0.0f, beta = 0.0f, d1 = 1.0f;
+    for (int t = 0; t <= T; ++t) {
+        const int nr = t > 0 ? nq : 0;       // read chunks of token t-1
+        const int nkk = t < T ? 2 * nk : 0;  // retrieve and write chunks of token t
+        const int jobs = nr + nkk;
+        const int64_t tsk = ts0 + (int64_t)t * a.tstride;  // token t's row of the inputs
+        if (t > 0) {
+            // token t-1's writes are done (every thread passed its last job before this barrier), so
+            // the write side is free for token t's, and token t-1's read side has landed
+            cp_async_wait_all();
             __syncthreads();
-            const int st = q % NS, c = q % nk, r0 = c * CH, n = min(CH, W - r0);
-            if (active) {
-                if (q < nk) {
-                    for (int r = 0; r < n; ++r) acc = fmaf(f2lo(aw2[r0 + r]), at(st, r), acc);
-                } else {
-                    if (q == nk) delta = __fmul_rn(beta, __fsub_rn(vr, acc));
-                    for (int r = 0; r < n; ++r) {
-                        const int w = r0 + r;
-                        const float y = fmaf(f2lo(kv2[w]), delta, __fmul_rn(at(st, r), G == 1 ? dsh : f2lo(dw2[w])));
-                        *reinterpret_cast<float*>(bank + koff[w] + jb) = y;
-                    }
+            wide_derive_q<I>(a, c0, L, smem);
+            if (t < T) {
+                wide_load_k<I>(a, tsk, L, smem);
+                cp_async_commit();  // the oldest group: landed once job 0 has
+                if (kd < 1) {       // few read chunks: the first write-row copy is in the ring's prologue
+                    cp_async_wait_all();
+                    __syncthreads();
+                    wide_derive_k<I>(a, c0, L, smem);
                 }
             }
             __syncthreads();
         }
-
-        const bool more = t + 1 < a.T;
-        if (more) {
-            prefetch_meta<I>(a, ts + a.tstride, L, smem);
-            if (G == 1 && tid == 0)
-                *reinterpret_cast<float*>(smem + L.dnext) = gate(__ldg(a.g + ts + a.tstride));
-        }
-        float racc = 0.0f;
-        for (int q = 0; q < NS - 1; ++q) {
-            if (q < nq)
-                ldgsts_chunk<float>(ring + (q % NS) * stage_bytes, bank, qoff, q * CH, min(CH, R - q * CH), sw, row_bytes);
-            else
+        const bool k_ready = t == 0 || kd < 1;  // token t's write side derived before the jobs
+        const auto load_token_state = [&]() {
+            if (active) vr = __ldg(a.v + tsk * hd + c0 + tid);
+            beta = *reinterpret_cast<const float*>(smem + L.beta);
+            d1 = dw[0];
+            acc = 0.0f;
+        };
+        if (t < T && k_ready) load_token_state();
+        const auto issue = [&](int q) {
+            if (q < jobs) {
+                unsigned char* dst = ring + (q % NS) * stage_bytes;
+                if (q < nr) {
+                    const int r0 = q * CH;
+                    ldgsts_rows<float>(reinterpret_cast<float*>(dst), bank, qoff + r0, min(CH, R - r0), sw, row_bytes);
+                } else {
+                    const int r0 = ((q - nr) % nk) * CH;
+                    ldgsts_rows<float>(reinterpret_cast<float*>(dst), bank, koff + r0, min(CH, W - r0), sw, row_bytes);
+                }
+            } else {
+                cp_async_commit();  // one group per job, so that the waits below count jobs
+            }
+        };
+        for (int q = 0; q < NS - 1; ++q) issue(q);
+        // Once token t-1's read rows are all consumed (the first job after them), token t's read side
+        // is copied in place; its commit group then sits among the ring's.
+        const int meta_job = t < T ? nr : -1;
+        for (int q = 0; q < jobs; ++q) {
+            if (t < T && !k_ready && q == kd) {  // token t's write side has landed (job 0 waited for it)
+                wide_derive_k<I>(a, c0, L, smem);
+                __syncthreads();
+                load_token_state();
+            }
+            // refill the stage that job q-1 used (every thread is done with it: the barrier that
+            // ends job q-1), so that all NS stages are in flight while job q is awaited
+            issue(q + NS - 1);
+            if (q == meta_job) {
+                wide_load_q<I>(a, tsk, L, smem);
                 cp_async_commit();
-        }
-        for (int q = 0; q < nq; ++q) {
-            const int qn = q + NS - 1;
-            if (qn < nq)
-                ldgsts_chunk<float>(ring + (qn % NS) * stage_bytes, bank, qoff, qn * CH, min(CH, R - qn * CH), sw, row_bytes);
+            }
+            // job q has landed: at most NS - 1 younger groups pending, one more while the metadata
+            // group committed after job q's is among them
+            if (meta_job >= 0 && q >= meta_job && q <= meta_job + NS - 1)
+                asm volatile("cp.async.wait_group %0;" ::"n"(NS) : "memory");
             else
-                cp_async_commit();
-            asm volatile("cp.async.wait_group %0;" ::"n"(NS - 1) : "memory");
-            __syncthreads();
-            const int st = q % NS, r0 = q * CH, n = min(CH, R - r0);
-            if (active)
-                for (int r = 0; r < n; ++r) racc = fmaf(f2lo(qv2[r0 + r]), at(st, r), racc);
-            __syncthreads();
+                asm volatile("cp.async.wait_group %0;" ::"n"(NS - 1) : "memory");
+            __syncthreads();  // job q is visible to every thread
+            // this thread's column of the chunk's rows; chunk heights are a multiple of 4, so the
+            // per-row metadata of four rows is one 16-byte load
+            const float* x = reinterpret_cast<const float*>(ring + (q % NS) * stage_bytes) + tid;
+            if (q < nr) {  // readings of token t-1
+                const int r0 = q * CH, n = min(CH, R - r0);
+                if (active) {
+                    int r = 0;
+                    for (; r + 4 <= n; r += 4) {
+                        const float4 q4 = *reinterpret_cast<const float4*>(qv + r0 + r);
+                        racc = fmaf(q4.x, x[(r + 0) * sw], racc);
+                        racc = fmaf(q4.y, x[(r + 1) * sw], racc);
+                        racc = fmaf(q4.z, x[(r + 2) * sw], racc);
+                        racc = fmaf(q4.w, x[(r + 3) * sw], racc);
+                    }
+                    for (; r < n; ++r) racc = fmaf(qv[r0 + r], x[r * sw], racc);
+                    if (q == nr - 1) {
+                        out[(tsk - a.tstride) * hd + c0 + tid] = racc;
+                        racc = 0.0f;
+                    }
+                }
+            } else if (q < nr + nk) {  // retrieve of token t: a_w = kv_w * d_w, then the fma chain
+                const int r0 = (q - nr) * CH, n = min(CH, W - r0);
+                if (active) {
+                    int r = 0;
+                    for (; r + 4 <= n; r += 4) {
+                        const float4 k4 = *reinterpret_cast<const float4*>(kv + r0 + r);
+                        float4 d4 = make_float4(d1, d1, d1, d1);
+                        if (G != 1) d4 = *reinterpret_cast<const float4*>(dw + r0 + r);
+                        acc = fmaf(__fmul_rn(k4.x, d4.x), x[(r + 0) * sw], acc);
+                        acc = fmaf(__fmul_rn(k4.y, d4.y), x[(r + 1) * sw], acc);
+                        acc = fmaf(__fmul_rn(k4.z, d4.z), x[(r + 2) * sw], acc);
+                        acc = fmaf(__fmul_rn(k4.w, d4.w), x[(r + 3) * sw], acc);
+                    }
+                    for (; r < n; ++r) {
+                        const int w = r0 + r;
+                        acc = fmaf(__fmul_rn(kv[w], G == 1 ? d1 : dw[w]), x[r * sw], acc);
+                    }
+                }
+            } else {  // decay-and-write of token t
+                const int r0 = (q - nr - nk) * CH, n = min(CH, W - r0);
+                if (active) {
+                    if (r0 == 0) delta = __fmul_rn(beta, __fsub_rn(vr, acc));
+                    unsigned char* bj = bank + jb;
+                    int r = 0;
+                    for (; r + 4 <= n; r += 4) {
+                        const int w = r0 + r;
+                        const float4 k4 = *reinterpret_cast<const float4*>(kv + w);
+                        const longlong2 o01 = *reinterpret_cast<const longlong2*>(koff + w);
+                        const longlong2 o23 = *reinterpret_cast<const longlong2*>(koff + w + 2);
+                        float4 d4 = make_float4(d1, d1, d1, d1);
+                        if (G != 1) d4 = *reinterpret_cast<const float4*>(dw + w);
+                        *reinterpret_cast<float*>(bj + o01.x) = fmaf(k4.x, delta, __fmul_rn(x[(r + 0) * sw], d4.x));
+                        *reinterpret_cast<float*>(bj + o01.y) = fmaf(k4.y, delta, __fmul_rn(x[(r + 1) * sw], d4.y));
+                        *reinterpret_cast<float*>(bj + o23.x) = fmaf(k4.z, delta, __fmul_rn(x[(r + 2) * sw], d4.z));
+                        *reinterpret_cast<float*>(bj + o23.y) = fmaf(k4.w, delta, __fmul_rn(x[(r + 3) * sw], d4.w));
+                    }
+                    for (; r < n; ++r) {
+                        const int w = r0 + r;
+                        *reinterpret_cast<float*>(bj + koff[w]) =
+                            fmaf(kv[w], delta, __fmul_rn(x[r * sw], G == 1 ? d1 : dw[w]));
+                    }
+                }
+            }
+            __syncthreads();  // job q's stage is refilled by the next job's copy
         }
-        if (active) out[ts * hd + c0 + j] = racc;
-
-        cp_async_wait_all();
-        __syncthreads();
-        if (more) derive_meta<float, I>(a, c0, L, smem);
-        __syncthreads();
     }
 }
 
@@ -1159,32 +1341,85 @@ __global__ void __launch_bounds__(kMaxThreads) decode_simt_kernel(const DecodeAr
 
 enum Path { kSimt = 0, kStaged = 1, kStream = 2 };
 
-template <typename I, int NS>
-auto stream1_kernel() {
-    return decode_stream1_kernel<I, NS>;
-}
-
 template <typename I, bool PIECE>
 auto vec1_kernel() {
     return decode_vec1_kernel<I, PIECE>;
 }
 
+// the streaming kernel of a bank dtype: float32 banks a column per thread, bf16 banks column pairs
+template <typename E, typename I>
+auto stream_kernel(int ns) {
+    if constexpr (sizeof(E) == 4)
+        return ns == 3 ? decode_wide_kernel<I, 3> : decode_wide_kernel<I, 4>;
+    else
+        return ns == 3 ? decode_stream_kernel<E, I, 3> : decode_stream_kernel<E, I, 4>;
+}
+
 template <typename E, typename I>
 int launch_typed(int path, bool scalar, const DecodeArgs& a, dim3 grid, dim3 block, size_t smem, cudaStream_t stream) {
-    const auto kernel = path == kStaged
-                            ? ((sizeof(E) == 2 && scalar)
-                                   ? (a.piece_write ? vec1_kernel<I, true>() : vec1_kernel<I, false>())
-                                   : (a.piece_write ? decode_vec_kernel<E, I, true> : decode_vec_kernel<E, I, false>))
-                        : path == kStream
-                            ? ((sizeof(E) == 4 && scalar)  // a column per thread
-                                   ? (a.stream_stages == 3 ? stream1_kernel<I, 3>() : stream1_kernel<I, 4>())
-                                   : (a.stream_stages == 3 ? decode_stream_kernel<E, I, 3>
-                                                           : decode_stream_kernel<E, I, 4>))
-                                          : decode_simt_kernel<E, I>;
+    const auto kernel =
+        path == kStaged
+            ? ((sizeof(E) == 2 && scalar) ? (a.piece_write ? vec1_kernel<I, true>() : vec1_kernel<I, false>())
+                                          : (a.piece_write ? decode_vec_kernel<E, I, true> : decode_vec_kernel<E, I, false>))
+        : path == kStream ? stream_kernel<E, I>(a.stream_stages)
+                          : decode_simt_kernel<E, I>;
     const int rc = allow_smem(reinterpret_cast<const void*>(kernel), smem);  // before the occupancy query
     if (rc != 0) return rc;
     const int early = fits_one_wave(kernel, grid.x, (int)block.x, smem) ? 1 : 0;
     return launch_pdl(kernel, grid, block, smem, stream, a, early);
+}
+
+constexpr int kWideRowsMin = 12;  // chunk rows of the float32 streaming kernel, at least
+constexpr int kWideRowsMax = 32;  // and at most
+
+// Geometry of decode_wide_kernel: one block per (stream, slice of up to 256 columns), a column per
+// thread. Each block is a chain of dependent row fetches whose time per token is set by the round
+// trips its ring needs, so the rows its ring keeps in flight (ns stages of ch rows) matter most; more
+// blocks per SM then keep the SM's memory traffic going while one block waits at a barrier or drains
+// its ring. Among slices of 256, 128 and 64 columns (at most the row), take those that run the grid
+// in the fewest waves (blocks per SM bounded by registers; the ring as deep as a block's share of the
+// SM's shared memory allows, at least kWideRowsMin rows per stage), and among them the narrowest
+// whose ring holds at least 85 % of the deepest one's rows.
+struct WideGeometry {
+    int sw, ch, ns;
+};
+
+WideGeometry pick_wide(const DecodeArgs& a) {
+    const int sms = sm_count();
+    const size_t smem_sm = smem_per_sm(), reserve = smem_reserved_per_block();
+    const int most = std::min(kWideRowsMax, std::max(std::max(a.W, a.R), kWideRowsMin));
+    const int full = std::min(a.hd, 256) / 4 * 4;
+    WideGeometry cand[3];
+    int64_t waves[3];
+    int n = 0;
+    for (int w0 : {256, 128, 64}) {
+        const int w = std::min(w0, full);
+        if (w0 < 256 && w < w0) continue;  // the narrower row is covered by the wider candidate
+        const int64_t nb = a.n_streams * ((a.hd + w - 1) / w);
+        const size_t meta = WideLayout(a.W, a.R, a.G, w, 0, 4).total;
+        int64_t per_sm = std::min<int64_t>((nb + sms - 1) / sms, 65536 / (((w + 31) / 32 * 32) * kWideRegs));
+        int ns = 4, ch = 0;
+        for (; per_sm >= 1; --per_sm) {  // as many blocks per SM as leave each a ring of kWideRowsMin rows
+            const size_t budget = smem_sm / (size_t)per_sm;
+            if (budget <= meta + reserve) continue;
+            const int64_t rows = (int64_t)((budget - meta - reserve) / ((size_t)w * 4));
+            ns = rows / 3 >= kTallChunk ? 3 : 4;
+            ch = (int)std::min<int64_t>(rows / ns, most) / 4 * 4;
+            if (ch >= kWideRowsMin) break;
+        }
+        if (per_sm < 1) continue;
+        cand[n] = WideGeometry{w, ch, ns};
+        waves[n++] = (nb + per_sm * sms - 1) / (per_sm * sms);
+    }
+    if (n == 0) return WideGeometry{full, kWideRowsMin, 4};
+    int64_t fewest = waves[0];
+    int deepest = 0;
+    for (int i = 0; i < n; ++i) fewest = std::min(fewest, waves[i]);
+    for (int i = 0; i < n; ++i)
+        if (waves[i] == fewest) deepest = std::max(deepest, cand[i].ns * cand[i].ch);
+    for (int i = n - 1; i >= 0; --i)  // candidates run from the widest slice to the narrowest
+        if (waves[i] == fewest && 20 * cand[i].ns * cand[i].ch >= 17 * deepest) return cand[i];
+    return cand[0];
 }
 
 int shrink_cols(int sw, int q) {
@@ -1231,7 +1466,15 @@ int launch_decode(const DecodeArgs& a0, int bank_dtype, int idx_dtype, cudaStrea
     a.piece_write = blocks >= 4LL * sm_count() ? 1 : 0;
     a.stream_rows = kStreamRowsMin;
     a.stream_stages = 4;
-    if (streamed) {
+    if (streamed && es == 4) {  // float32: the slice geometry of decode_wide_kernel
+        const WideGeometry g = pick_wide(a);
+        sw = g.sw;
+        a.stream_rows = g.ch;
+        a.stream_stages = g.ns;
+        a.slice_cols = sw;
+        a.n_slices = (a.hd + sw - 1) / sw;
+        if (a.n_streams * a.n_slices > INT_MAX) return SDM_ECOUNT;
+    } else if (streamed) {
         // the largest chunk that keeps the whole grid resident in one wave, for slices of w columns
         // and a ring of ns chunks
         const auto chunk_rows = [&](int w, int64_t nb, int ns) {
@@ -1277,17 +1520,18 @@ int launch_decode(const DecodeArgs& a0, int bank_dtype, int idx_dtype, cudaStrea
     }
     const int64_t blocks_final = a.n_streams * a.n_slices;
     const int path = !vec ? kSimt : streamed ? kStream : kStaged;
-    // One column per thread (scalar chains, twice the warps): float32 streaming over slices of up
-    // to 128 columns (wider slices keep column pairs: blocks of 256 threads measured slower), and
-    // bf16 staged slices of up to 64 columns, the narrow slices of grids with few streams, which
+    // One column per thread (scalar chains, twice the warps): float32 streaming (decode_wide_kernel),
+    // and bf16 staged slices of up to 64 columns, the narrow slices of grids with few streams, which
     // wait on latency and gain from the extra warps (full 256-byte rows of many streams keep
     // column pairs: 7 % faster there).
-    const bool scalar = (path == kStream && es == 4 && sw <= 128) || (path == kStaged && es == 2 && sw <= 64);
+    const bool scalar = (path == kStream && es == 4) || (path == kStaged && es == 2 && sw <= 64);
     const int tcols = scalar ? 1 : cpt;
     const int threads = ((sw + tcols - 1) / tcols + 31) / 32 * 32;
-    const size_t smem = path == kStaged   ? VecLayout(a.W, a.R, a.G, sw, es, is).total
-                        : path == kStream ? StreamLayout(a.W, a.R, a.G, sw, es, is, a.stream_rows, a.stream_stages).total
-                                          : SimtLayout(a.W, a.R, sw, es).total;
+    const size_t smem = path == kStaged ? VecLayout(a.W, a.R, a.G, sw, es, is).total
+                        : path == kStream
+                            ? (es == 4 ? WideLayout(a.W, a.R, a.G, sw, a.stream_rows, a.stream_stages).total
+                                       : StreamLayout(a.W, a.R, a.G, sw, es, is, a.stream_rows, a.stream_stages).total)
+                            : SimtLayout(a.W, a.R, sw, es).total;
 
     const dim3 grid((unsigned)blocks_final), block((unsigned)threads);
     if (bank_dtype == SDM_BF16) {

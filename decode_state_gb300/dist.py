@@ -1,8 +1,9 @@
-"""Multi-process plumbing for weak scaling: one process per GPU, launched by torch.distributed.run.
+"""Multi-process plumbing: one process per GPU, launched by torch.distributed.run.
 
-The SDM workloads shard without any exchange: decode streams own private bank rows and gather
-tokens are independent, so every rank runs its own shard (its own bank and inputs) and the only
-collectives are the host-side barrier and the max-over-ranks of the timed region.
+The SDM decode shards without any exchange: streams own private bank rows, so a job of S streams
+splits into contiguous stream ranges, each rank holding its streams' bank rows and inputs and
+running the same kernel on them (stream_shard). The only collectives are the host-side barrier
+and the max-over-ranks of the timed region.
 """
 
 from __future__ import annotations
@@ -63,7 +64,7 @@ def sum_over_ranks(r: Rank, value: float, device=None) -> float:
 
 
 def shard_seed(base_seed: int, r: Rank) -> int:
-    """Each rank draws its own shard of streams (or tokens) from its own seed."""
+    """A seed of this rank's own, for workloads that are not split (each rank draws its own)."""
     return base_seed + 1000003 * r.rank
 
 
@@ -72,6 +73,14 @@ def shard_range(n: int, r: Rank) -> tuple[int, int]:
     base, extra = divmod(n, r.world)
     lo = r.rank * base + min(r.rank, extra)
     return lo, lo + base + (1 if r.rank < extra else 0)
+
+
+def stream_shard(n_streams: int, r: Rank, block: int) -> tuple[int, int]:
+    """This rank's streams [lo, hi) of an n_streams job split on `block`-stream boundaries: the
+    blocks are split as evenly as shard_range splits units (the last block may be shorter)."""
+    nb = (n_streams + block - 1) // block
+    b0, b1 = shard_range(nb, r)
+    return min(b0 * block, n_streams), min(b1 * block, n_streams)
 
 
 def shutdown(r: Rank):

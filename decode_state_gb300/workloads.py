@@ -172,6 +172,40 @@ def make_decode_inputs(wl: DecodeWorkload, device="cpu", seed: int | None = None
                 q_idx=q_idx, q_val=q_val.contiguous())
 
 
+SHARD_BLOCK = 64  # streams per independently seeded block of a partitioned decode workload
+
+
+def shard_blocks(n_streams: int, block: int = SHARD_BLOCK) -> int:
+    return (n_streams + block - 1) // block
+
+
+def make_decode_shard(wl: DecodeWorkload, lo: int, hi: int, device="cpu", seed: int | None = None,
+                      block: int = SHARD_BLOCK) -> dict:
+    """Streams [lo, hi) of decode workload ``wl`` drawn as one job that any set of processes can
+    split: the job's streams form blocks of ``block`` streams (the last may be shorter), block b
+    drawn by make_decode_inputs from its own seed (seed + 7919 * b), with its slots offset to the
+    block's own bank rows. ``lo`` and ``hi`` must be block boundaries (or n_streams). Returns the
+    shard with the layout of make_decode_inputs over hi - lo streams: its bank holds the shard's
+    rows [lo * P, hi * P) of the job's bank, and its slots are rebased to that local bank."""
+    seed = wl.seed if seed is None else seed
+    if lo % block or (hi % block and hi != wl.n_streams) or not 0 <= lo <= hi <= wl.n_streams:
+        raise ValueError(f"shard [{lo}, {hi}) is not on {block}-stream block boundaries of {wl.n_streams} streams")
+    parts = []
+    for b in range(lo // block, shard_blocks(hi, block)):
+        n = min(block, wl.n_streams - b * block)
+        x = make_decode_inputs(wl.scaled(n_streams=n), device=device, seed=seed + 7919 * b)
+        off = (b * block - lo) * wl.slots_per_stream  # the block's first row in the shard's bank
+        x["k_idx"] += off
+        x["q_idx"] += off
+        parts.append(x)
+    if not parts:
+        return make_decode_inputs(wl.scaled(n_streams=0), device=device, seed=seed)
+    out = {"bank": torch.cat([x["bank"] for x in parts])}
+    for k in ("k_idx", "k_val", "v", "beta", "g", "q_idx", "q_val"):
+        out[k] = torch.cat([x[k] for x in parts], dim=1).contiguous()
+    return out
+
+
 def make_gather_inputs(wl: GatherWorkload, device="cpu", seed: int | None = None) -> dict:
     """Draw one gather workload: bank, per-chunk valid counts, and one or two operands."""
     seed = wl.seed if seed is None else seed
