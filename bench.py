@@ -54,6 +54,9 @@ def parse_args():
                    help="workload of the timed step (default: the serving-scale decode)")
     p.add_argument("--streams", type=int, default=0, help="override the decode stream count (smaller cases)")
     p.add_argument("--tokens", type=int, default=0, help="override T (decode) or the token count (gather)")
+    p.add_argument("--gather-form", choices=("stash", "compact", "none"), default="stash",
+                   help="gather workloads: the stash (as the workload names it), a compact snapshot of operand 0 "
+                        "(sdm_gather_kpos) in its place, or outputs only")
     a = p.parse_args()
     a.warmup = max(3, a.warmup)
     a.steps = max(1, a.steps)
@@ -285,11 +288,15 @@ class Case:
             self.g = workloads.make_gather_inputs(wl, device=dev, seed=sdist.shard_seed(wl.seed, r))
             self.outs = [torch.empty((wl.tokens, wl.hd), device=dev) for _ in wl.widths]
             bdt = workloads.BANK_DTYPES[wl.bank_dtype]
-            self.stash = (torch.empty((wl.tokens, wl.widths[0], wl.hd), dtype=bdt, device=dev) if wl.stash else None)
+            self.form = args.gather_form if wl.stash else "none"
+            self.stash = (torch.empty((wl.tokens, wl.widths[0], wl.hd), dtype=bdt, device=dev)
+                          if self.form == "stash" else None)
+            self.kpos, self.compact, written = (compact_snapshot(wl, self.g, dev) if self.form == "compact"
+                                                else (None, None, 0))
             self.units = wl.tokens
             self.unit = "tokens/s"
             self.launches = 1
-            self.nbytes = workloads.gather_bytes(wl, self.g["chunk_valid"])
+            self.nbytes = gather_form_bytes(wl, self.g, self.form, written)
             self.kernel = f"gather_kernel<{wl.bank_dtype},{wl.idx_dtype},{wl.w_dtype},vector rows>"
             self.metric = "SDM token-gather tokens/sec and effective bank GB/s as fraction of GB300 HBM peak"
         self.wl = wl
@@ -306,7 +313,8 @@ class Case:
                 sdm.decode_step(self.x["bank"], *(self.x[k][t] for k in DECODE_KEYS), out=self.out[t])
         else:
             sdm.gather(self.g["bank"], self.g["ops"], chunk=wl.chunk, chunk_valid=self.g["chunk_valid"],
-                       stash=self.stash, outs=self.outs, with_stash=self.stash is not None)
+                       stash=self.stash, outs=self.outs, with_stash=self.stash is not None, kpos=self.kpos,
+                       compact=self.compact)
 
     def config(self, r: sdist.Rank) -> dict:
         wl = self.wl
@@ -315,7 +323,8 @@ class Case:
             gib = wl.n_slots * wl.hd * (2 if wl.bank_dtype == "bf16" else 4) / 2 ** 30
             return {"workload": wl.name, "n_slots": wl.n_slots, "head_dim": wl.hd, "tokens": wl.tokens,
                     "chunk": wl.chunk, "widths": list(wl.widths), "bank_dtype": wl.bank_dtype,
-                    "idx_dtype": wl.idx_dtype, "w_dtype": wl.w_dtype, "stash": wl.stash, "call": "sdm_gather",
+                    "idx_dtype": wl.idx_dtype, "w_dtype": wl.w_dtype, "stash": self.form == "stash",
+                    "form": self.form, "call": "sdm_gather_kpos" if self.form == "compact" else "sdm_gather",
                     "l2": f"inputs larger than L2 ({gib:.0f} GiB bank), no flush", "parallelism": par}
         call = {"decode_seq": "sdm_decode_seq", "decode_seq_stream_major": "sdm_decode_seq_ex (SDM_STREAM_MAJOR)",
                 "decode_step": "sdm_decode_step x T"}[self.kind]
@@ -370,6 +379,7 @@ class Case:
         else:
             g = self.g
             flat = [t for op in g["ops"] for t in op] + ([g["chunk_valid"]] if g["chunk_valid"] is not None else [])
+            flat += [self.kpos] if self.kpos is not None else []
             host_in = [t.cpu().pin_memory() for t in flat]
             dev_in = [torch.empty_like(t) for t in flat]
             host_outs = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in self.outs]
@@ -381,8 +391,9 @@ class Case:
                     d.copy_(h, non_blocking=True)
                 ops = [(dev_in[2 * o], dev_in[2 * o + 1]) for o in range(n_ops)]
                 cv = dev_in[2 * n_ops] if g["chunk_valid"] is not None else None
+                kp = dev_in[-1] if self.kpos is not None else None
                 sdm.gather(g["bank"], ops, chunk=wl.chunk, chunk_valid=cv, stash=self.stash, outs=self.outs,
-                           with_stash=self.stash is not None)
+                           with_stash=self.stash is not None, kpos=kp, compact=self.compact)
                 for h, o in zip(host_outs, self.outs):
                     h.copy_(o, non_blocking=True)
         h2d = sum(t.numel() * t.element_size() for t in host_in)
@@ -424,7 +435,8 @@ class Case:
                 d, t = oracle_gather_tokens(bank_h, self.g, order[i:i + 256].tolist(), self.wl.chunk)
                 done, secs, i = done + d, secs + t, i + 256
             sample = (f"{done} of {self.wl.tokens} tokens of the benchmark's own inputs "
-                      f"(padding included, {secs:.1f} s single-threaded)")
+                      f"(padding included, {secs:.1f} s single-threaded"
+                      + ("" if self.form == "stash" else "; the oracle's outputs-and-stash form") + ")")
         return {"value": done / secs, "unit": self.unit, "cores": 1, "kind": "oracle", "sample": sample}
 
     def cpu_baseline_all_cores(self, budget_s: float, single: dict):
@@ -642,14 +654,11 @@ def plan_slabs(dev, slab: int = 256) -> dict:
     return res
 
 
-def kpos_gather(dev, peak: float) -> dict:
-    """The gather workload with a compact snapshot (sdm_gather_kpos) in place of the stash: operand
-    0's rows are stored once per chunk, at the first position of each distinct row among the
-    chunk's sorted entries (kpos, prepared here on the device before timing)."""
-    from decode_state_gb300 import sdm
-
-    wl = workloads.C4
-    g = workloads.make_gather_inputs(wl, device=dev)
+def compact_snapshot(wl, g: dict, dev):
+    """Inputs of the compact-snapshot form of a gather workload: operand 0's rows are stored once
+    per chunk, at the first position of each distinct row among the chunk's sorted entries. Returns
+    (kpos [tokens, W0] int32, the zeroed snapshot [chunks, chunk * W0, hd], rows written by live
+    tokens), prepared on the device."""
     idx0 = g["ops"][0][0]
     W0, n_chunks = idx0.shape[1], wl.tokens // wl.chunk
     ent = idx0.view(n_chunks, wl.chunk * W0)
@@ -661,12 +670,30 @@ def kpos_gather(dev, peak: float) -> dict:
     kpos = torch.empty_like(srt).scatter_(1, order, torch.where(first, first_pos, torch.full_like(pos, -1)))
     kpos = kpos.view(wl.tokens, W0).to(torch.int32)
     compact = torch.zeros((n_chunks, wl.chunk * W0, wl.hd), dtype=workloads.BANK_DTYPES[wl.bank_dtype], device=dev)
-    outs = [torch.empty((wl.tokens, wl.hd), device=dev) for _ in wl.widths]
     live = (torch.arange(wl.tokens, device=dev) % wl.chunk) < g["chunk_valid"].repeat_interleave(wl.chunk)
-    es = 2 if wl.bank_dtype == "bf16" else 4
     written = int(((kpos >= 0) & live[:, None]).sum().item())
-    nbytes = (int(live.sum().item()) * sum(wl.widths) * wl.hd * es + written * wl.hd * es
-              + wl.tokens * len(wl.widths) * wl.hd * 4)
+    return kpos, compact, written
+
+
+def gather_form_bytes(wl, g: dict, form: str, written: int = 0) -> int:
+    """Algorithmic bytes of one gather call in the given form: the workload's own (stash), or
+    live-token row reads and outputs plus the compact rows written (compact), or without them (none)."""
+    if form == "stash":
+        return workloads.gather_bytes(wl, g["chunk_valid"])
+    es = 2 if wl.bank_dtype == "bf16" else 4
+    live = int(g["chunk_valid"].to(torch.int64).sum().item()) if g["chunk_valid"] is not None else wl.tokens
+    return live * sum(wl.widths) * wl.hd * es + written * wl.hd * es + wl.tokens * len(wl.widths) * wl.hd * 4
+
+
+def kpos_gather(dev, peak: float) -> dict:
+    """The gather workload with a compact snapshot (sdm_gather_kpos) in place of the stash."""
+    from decode_state_gb300 import sdm
+
+    wl = workloads.C4
+    g = workloads.make_gather_inputs(wl, device=dev)
+    kpos, compact, written = compact_snapshot(wl, g, dev)
+    outs = [torch.empty((wl.tokens, wl.hd), device=dev) for _ in wl.widths]
+    nbytes = gather_form_bytes(wl, g, "compact", written)
 
     def step():
         sdm.gather(g["bank"], g["ops"], chunk=wl.chunk, chunk_valid=g["chunk_valid"], kpos=kpos, compact=compact,

@@ -946,6 +946,8 @@ __global__ void __launch_bounds__(kMaxThreads, 1) decode_stream_kernel(const Dec
 // is refilled as soon as every thread has consumed it, before the next chunk is awaited, so that
 // all NS stages are in flight during each wait.
 // Chunks are consumed in ascending row order, so every sum keeps the staged path's order and bits.
+// The readings and the written-back rows are stored evict-first in L2: what L2 should keep are the
+// write rows between their two passes and the rows warmed for the next copies.
 
 struct WideLayout {
     size_t koff, kv, dw, beta, qoff, qv, ring, total;
@@ -1190,7 +1192,7 @@ __global__ void __launch_bounds__(kMaxThreads, 65536 / (kMaxThreads * kWideRegs)
                     }
                     for (; r < n; ++r) racc = fmaf(qv[r0 + r], x[r * sw], racc);
                     if (q == nr - 1) {
-                        out[(tsk - a.tstride) * hd + c0 + tid] = racc;
+                        st_hint(out + (tsk - a.tstride) * hd + c0 + tid, racc, l2_evict_first());
                         racc = 0.0f;
                     }
                 }
@@ -1225,15 +1227,16 @@ __global__ void __launch_bounds__(kMaxThreads, 65536 / (kMaxThreads * kWideRegs)
                         const longlong2 o23 = *reinterpret_cast<const longlong2*>(koff + w + 2);
                         float4 d4 = make_float4(d1, d1, d1, d1);
                         if (G != 1) d4 = *reinterpret_cast<const float4*>(dw + w);
-                        *reinterpret_cast<float*>(bj + o01.x) = fmaf(k4.x, delta, __fmul_rn(x[(r + 0) * sw], d4.x));
-                        *reinterpret_cast<float*>(bj + o01.y) = fmaf(k4.y, delta, __fmul_rn(x[(r + 1) * sw], d4.y));
-                        *reinterpret_cast<float*>(bj + o23.x) = fmaf(k4.z, delta, __fmul_rn(x[(r + 2) * sw], d4.z));
-                        *reinterpret_cast<float*>(bj + o23.y) = fmaf(k4.w, delta, __fmul_rn(x[(r + 3) * sw], d4.w));
+                        const uint64_t ef = l2_evict_first();
+                        st_hint(reinterpret_cast<float*>(bj + o01.x), fmaf(k4.x, delta, __fmul_rn(x[(r + 0) * sw], d4.x)), ef);
+                        st_hint(reinterpret_cast<float*>(bj + o01.y), fmaf(k4.y, delta, __fmul_rn(x[(r + 1) * sw], d4.y)), ef);
+                        st_hint(reinterpret_cast<float*>(bj + o23.x), fmaf(k4.z, delta, __fmul_rn(x[(r + 2) * sw], d4.z)), ef);
+                        st_hint(reinterpret_cast<float*>(bj + o23.y), fmaf(k4.w, delta, __fmul_rn(x[(r + 3) * sw], d4.w)), ef);
                     }
                     for (; r < n; ++r) {
                         const int w = r0 + r;
-                        *reinterpret_cast<float*>(bj + koff[w]) =
-                            fmaf(kv[w], delta, __fmul_rn(x[r * sw], G == 1 ? d1 : dw[w]));
+                        st_hint(reinterpret_cast<float*>(bj + koff[w]),
+                                fmaf(kv[w], delta, __fmul_rn(x[r * sw], G == 1 ? d1 : dw[w])), l2_evict_first());
                     }
                 }
             }

@@ -7,17 +7,19 @@
 // and a token whose position in its chunk is >= valid is padding: it reads nothing and gets zero
 // outputs and zero stash rows.
 //
-// Design. One block owns one (token, column slice). Every thread issues 16-byte cp.async copies
-// of the entry row slices of both operands (all in flight at once) into shared memory; the stash
+// Design. One block owns one (token, column slice, operand): two small blocks per token rather
+// than one block over both operands keep twice the independent chains (index load, then rows)
+// resident per SM in the same shared memory. Every thread issues 16-byte cp.async copies of the
+// operand's entry row slices (all in flight at once) into shared memory; the stash
 // rows then leave shared memory by bulk stores (one cp.async.bulk store for the whole token when
-// the slice is the full row) while each thread reduces its column over the entries in ascending
-// order with fmaf (the reference's order with one row group). One column per thread (rather than
-// a bf16 pair) gives twice the warps for the reductions; the full gather workload measured 6 %
-// faster that way. The row loads use 16-byte
-// copies rather than one bulk copy per row: with 256-byte rows the bulk-copy engine sustained
-// about 3 TB/s of row reads per GPU. Rows that are not a multiple of 16 bytes, or an unaligned
-// bank, take a plain-load path with one column per thread. Row indices outside [0, n_slots) are
-// skipped (zero row) and flagged in the status word.
+// the slice is the full row, its lines marked evict-first in L2: the kernel never reads them),
+// while each thread reduces its column over the entries in ascending order with fmaf (the
+// reference's order with one row group). One column per thread (rather than a bf16 pair) gives
+// twice the warps for the reductions; the full gather workload measured 6 % faster that way. The
+// row loads use 16-byte copies rather than one bulk copy per row: with 256-byte rows the bulk-copy
+// engine sustained about 3 TB/s of row reads per GPU. Rows that are not a multiple of 16 bytes, or
+// an unaligned bank, take a plain-load path with one column per thread. Row indices outside
+// [0, n_slots) are skipped (zero row) and flagged in the status word.
 //
 // Compact-snapshot form (kpos set): instead of the stash, operand 0's row of entry n goes to row
 // kpos[t, n] of the chunk's block of chunk * W0 rows when kpos >= 0; each thread stores the 16-byte
@@ -44,26 +46,62 @@ struct GatherLayout {
     __host__ __device__ GatherLayout(int n_rows, int slice_cols, int es) {
         rows = 0;
         slot = align_up((size_t)n_rows * slice_cols * es, 16);
-        wt = slot + (size_t)n_rows * 8;
-        kp = wt + (size_t)n_rows * 4;  // compact-snapshot rows of operand 0's entries
+        wt = align_up(slot + (size_t)n_rows * 8, 16);  // float weights, or raw bf16 ones
+        kp = align_up(wt + (size_t)n_rows * 4, 16);    // compact-snapshot rows of operand 0's entries
         total = kp + (size_t)n_rows * 4;
     }
 };
 
-template <typename WT>
-__device__ __forceinline__ float load_weight(const void* p, int64_t i) {
-    return to_f32(__ldg(static_cast<const WT*>(p) + i));
+// bf16 weights over a bf16 bank stay raw: both operands of the mixed-precision fma below
+template <typename E, typename WT>
+constexpr bool kRawWeights = sizeof(E) == 2 && sizeof(WT) == 2;
+
+// acc + w * x for bf16 w and x: the product of two bf16 values is exact in float32, so this single
+// rounding gives the same float32 as widening both and calling fmaf
+__device__ __forceinline__ float fma_bf16(uint16_t w, uint16_t x, float acc) {
+    asm("fma.rn.f32.bf16 %0, %1, %2, %0;" : "+f"(acc) : "h"(w), "h"(x));
+    return acc;
 }
 
-// Zero this block's slice of the outputs and stash rows of padding token t.
-template <typename E>
-__device__ void write_padding(const GatherArgs& a, int64_t t, int c0, int ncols, int j, bool active, bool flat16) {
-    const int hd = a.hd, W0 = a.width[0];
-    if (active) {
-        a.out[0][t * hd + c0 + j] = 0.0f;
-        if (a.n_ops == 2) a.out[1][t * hd + c0 + j] = 0.0f;
+// one column's weighted sum over the NR staged rows (x: the column's element of row 0, rows sw
+// elements apart), one chain over ascending entries
+template <typename E, typename WT>
+__device__ __forceinline__ float weighted_sum(const E* x, int sw, const unsigned char* wts, int NR) {
+    float acc = 0.0f;
+    int n = 0;
+    if constexpr (kRawWeights<E, WT>) {
+        const uint16_t* w = reinterpret_cast<const uint16_t*>(wts);
+        for (; n + 8 <= NR; n += 8) {
+            const uint4 w8 = *reinterpret_cast<const uint4*>(w + n);
+            const uint32_t wp[4] = {w8.x, w8.y, w8.z, w8.w};
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                acc = fma_bf16((uint16_t)(wp[u] & 0xffffu), x[(size_t)(n + 2 * u) * sw], acc);
+                acc = fma_bf16((uint16_t)(wp[u] >> 16), x[(size_t)(n + 2 * u + 1) * sw], acc);
+            }
+        }
+        for (; n < NR; ++n) acc = fma_bf16(w[n], x[(size_t)n * sw], acc);
+    } else {
+        const float* w = reinterpret_cast<const float*>(wts);
+        for (; n + 4 <= NR; n += 4) {
+            const float4 w4 = *reinterpret_cast<const float4*>(w + n);
+            acc = fmaf(w4.x, to_f32(x[(size_t)(n + 0) * sw]), acc);
+            acc = fmaf(w4.y, to_f32(x[(size_t)(n + 1) * sw]), acc);
+            acc = fmaf(w4.z, to_f32(x[(size_t)(n + 2) * sw]), acc);
+            acc = fmaf(w4.w, to_f32(x[(size_t)(n + 3) * sw]), acc);
+        }
+        for (; n < NR; ++n) acc = fmaf(w[n], to_f32(x[(size_t)n * sw]), acc);
     }
-    if (a.stash == nullptr || a.kpos != nullptr) return;  // the compact snapshot takes nothing from padding
+    return acc;
+}
+
+// Zero this block's slice of operand op's output, and for operand 0 its stash rows, of padding
+// token t.
+template <typename E>
+__device__ void write_padding(const GatherArgs& a, int64_t t, int op, int c0, int j, bool active, bool flat16) {
+    const int hd = a.hd, W0 = a.width[0];
+    if (active) a.out[op][t * hd + c0 + j] = 0.0f;
+    if (op != 0 || a.stash == nullptr || a.kpos != nullptr) return;  // the compact snapshot takes nothing from padding
     E* st = static_cast<E*>(a.stash) + t * W0 * hd;
     if (flat16) {  // the token's whole stash block is contiguous and 16-byte aligned
         uint4* p = reinterpret_cast<uint4*>(st);
@@ -80,16 +118,20 @@ __global__ void __launch_bounds__(kMaxThreads) gather_kernel(const GatherArgs a,
     extern __shared__ __align__(128) unsigned char smem[];
 
     const int hd = a.hd, sw = a.slice_cols;
-    const int W0 = a.width[0], W1 = a.n_ops == 2 ? a.width[1] : 0, NR = W0 + W1;
-    const GatherLayout L(NR, sw, ES);
+    const int W0 = a.width[0], W1 = a.n_ops == 2 ? a.width[1] : 0;
+    // one block per (token, column slice, operand): operand op's NR entries
+    const int op = (int)(blockIdx.x % a.n_ops);
+    const unsigned bx = blockIdx.x / a.n_ops;
+    const int NR = op ? W1 : W0;
+    const GatherLayout L(max(W0, W1), sw, ES);
     E* rows = reinterpret_cast<E*>(smem + L.rows);
     int64_t* slot = reinterpret_cast<int64_t*>(smem + L.slot);
-    float* wt = reinterpret_cast<float*>(smem + L.wt);
+    unsigned char* wt = smem + L.wt;
     int* kp = reinterpret_cast<int*>(smem + L.kp);
 
     const int tid = threadIdx.x, nt = blockDim.x;
-    const int64_t t = blockIdx.x / a.n_slices;
-    const int c0 = (int)(blockIdx.x % a.n_slices) * sw;
+    const int64_t t = bx / a.n_slices;
+    const int c0 = (int)(bx % a.n_slices) * sw;
     const int ncols = min(sw, hd - c0);
     const int j = tid;  // this thread's column within the slice
     const bool active = j < ncols;
@@ -113,22 +155,24 @@ __global__ void __launch_bounds__(kMaxThreads) gather_kernel(const GatherArgs a,
             grid_dependency_wait();
             if (early_trigger) grid_launch_dependents();
         }
-        write_padding<E>(a, t, c0, ncols, j, active, stash_bulk && a.n_slices == 1);
+        write_padding<E>(a, t, op, c0, j, active, stash_bulk && a.n_slices == 1);
         return;
     }
 
-    // entries of both operands: operand 0 in [0, W0), operand 1 in [W0, NR)
+    // this operand's entries
     for (int e = tid; e < NR; e += nt) {
-        const bool op1 = e >= W0;
-        const int64_t i = op1 ? t * W1 + (e - W0) : t * W0 + e;
-        int64_t sl = load_index<I>(op1 ? a.idx[1] : a.idx[0], i);
+        const int64_t i = t * NR + e;
+        int64_t sl = load_index<I>(a.idx[op], i);
         if (sl < 0 || sl >= a.n_slots) {
             atomicOr(&g_gather_status, SDM_DEV_BAD_INDEX);
             sl = -1;
         }
         slot[e] = sl;
-        wt[e] = load_weight<WT>(op1 ? a.w[1] : a.w[0], i);
-        if (a.kpos != nullptr && !op1) {
+        if constexpr (kRawWeights<E, WT>)
+            reinterpret_cast<uint16_t*>(wt)[e] = __ldg(static_cast<const uint16_t*>(a.w[op]) + i);
+        else
+            reinterpret_cast<float*>(wt)[e] = to_f32(__ldg(static_cast<const WT*>(a.w[op]) + i));
+        if (a.kpos != nullptr && op == 0) {
             int k = __ldg(a.kpos + i);
             if (k >= a.chunk * W0 || (k >= 0 && sl < 0)) {
                 if (k >= a.chunk * W0) atomicOr(&g_gather_status, SDM_DEV_BAD_INDEX);
@@ -138,7 +182,8 @@ __global__ void __launch_bounds__(kMaxThreads) gather_kernel(const GatherArgs a,
         }
     }
     // compact snapshot: this token's chunk block
-    E* compact = a.kpos != nullptr ? stash + (t / a.chunk) * ((int64_t)a.chunk * W0) * hd : nullptr;
+    E* compact = a.kpos != nullptr && op == 0 ? stash + (t / a.chunk) * ((int64_t)a.chunk * W0) * hd : nullptr;
+    const bool stash_rows = stash != nullptr && a.kpos == nullptr && op == 0;
     __syncthreads();
     if (a.inputs_ready) {
         const unsigned char* src = reinterpret_cast<const unsigned char*>(bank) + (int64_t)c0 * ES;
@@ -177,7 +222,7 @@ __global__ void __launch_bounds__(kMaxThreads) gather_kernel(const GatherArgs a,
         asm volatile("cp.async.commit_group;\n\tcp.async.wait_all;" ::: "memory");
         if (compact != nullptr) {  // this thread's own landed pieces of operand 0's named rows
             const auto put = [&](int e, int k) {
-                if (e < W0 && kp[e] >= 0)
+                if (kp[e] >= 0)
                     *reinterpret_cast<uint4*>(reinterpret_cast<unsigned char*>(compact) + kp[e] * rowb + c0 * ES +
                                               k * 16) = *reinterpret_cast<const uint4*>(dst + e * rs + k * 16);
             };
@@ -191,12 +236,12 @@ __global__ void __launch_bounds__(kMaxThreads) gather_kernel(const GatherArgs a,
         fence_proxy_async_shared();  // the rows are read by bulk stores (async proxy) below
         __syncthreads();
         // stash: raw rows of operand 0 straight from shared memory
-        if (stash != nullptr && compact == nullptr) {
+        if (stash_rows) {
             if (stash_bulk) {
                 if (a.n_slices == 1) {
                     if (tid == 0) {
                         fence_proxy_async_shared();
-                        bulk_s2g(stash + t * W0 * hd, rows, (uint32_t)W0 * hd * ES);
+                        bulk_s2g_hint(stash + t * W0 * hd, rows, (uint32_t)W0 * hd * ES, l2_evict_first());
                         bulk_commit();
                     }
                 } else if (tid < 32) {
@@ -229,22 +274,15 @@ __global__ void __launch_bounds__(kMaxThreads) gather_kernel(const GatherArgs a,
         if (compact != nullptr) {
             for (int n = 0; n < W0; ++n)
                 if (kp[n] >= 0) compact[(int64_t)kp[n] * hd + c0 + j] = rows[(size_t)n * sw + j];
-        } else if (stash != nullptr) {
+        } else if (stash_rows) {
             for (int n = 0; n < W0; ++n) stash[(t * W0 + n) * hd + c0 + j] = rows[(size_t)n * sw + j];
         }
     }
 
-    // weighted sums, one fmaf chain per column over ascending entries
-    if (active) {
-        for (int o = 0; o < a.n_ops; ++o) {
-            const int e0 = o ? W0 : 0, width = o ? W1 : W0;
-            float acc = 0.0f;
-            for (int n = 0; n < width; ++n) acc = fmaf(wt[e0 + n], to_f32(rows[(size_t)(e0 + n) * sw + j]), acc);
-            (o ? a.out[1] : a.out[0])[t * hd + c0 + j] = acc;
-        }
-    }
+    // the weighted sum, one fmaf chain per column over ascending entries
+    if (active) a.out[op][t * hd + c0 + j] = weighted_sum<E, WT>(rows + j, sw, wt, NR);
     // shared memory must outlive the bulk stores that read it
-    if (BULK && stash != nullptr && stash_bulk && (a.n_slices == 1 ? tid == 0 : tid < 32)) bulk_wait_read_all();
+    if (BULK && stash_rows && stash_bulk && (a.n_slices == 1 ? tid == 0 : tid < 32)) bulk_wait_read_all();
 }
 
 template <typename E, typename I, typename WT>
@@ -279,20 +317,20 @@ int plan_gather(const GatherArgs& a0, int bank_dtype, int idx_dtype, int w_dtype
     // snapshot (stored piece by piece) an aligned snapshot
     const bool bulk = ((int64_t)a.hd * es) % 16 == 0 && reinterpret_cast<uintptr_t>(a.bank) % 16 == 0 &&
                       (a.kpos == nullptr || reinterpret_cast<uintptr_t>(a.stash) % 16 == 0);
-    const int n_rows = a.width[0] + (a.n_ops == 2 ? a.width[1] : 0);
+    const int n_rows = std::max(a.width[0], a.n_ops == 2 ? a.width[1] : 0);  // rows of one block
 
     int sw = std::min(a.hd, kMaxThreads);  // one column per thread
     if (bulk) sw = sw / (16 / es) * (16 / es);
     while ((size_t)n_rows * sw * es > kRowsBudget && sw > (bulk ? 16 / es : 32)) sw = shrink_cols(sw, bulk, es);
     a.slice_cols = sw;
     a.n_slices = (a.hd + sw - 1) / sw;
-    const int64_t blocks = a.tokens * a.n_slices;
+    const int64_t blocks = a.tokens * a.n_slices * a.n_ops;
     if (blocks > INT_MAX) return SDM_ECOUNT;
     L->stash_bulk =
         a.stash != nullptr && a.kpos == nullptr && reinterpret_cast<uintptr_t>(a.stash) % 16 == 0 && bulk;
     L->grid = (unsigned)blocks;
     L->block = (unsigned)((sw + 31) / 32 * 32);
-    L->smem = GatherLayout(n_rows, sw, es).total;
+    L->smem = GatherLayout(n_rows, sw, es).total;  // the wider operand's rows
     if (bank_dtype == SDM_BF16) {
         if (idx_dtype == SDM_I32)
             resolve_w<uint16_t, int32_t>(w_dtype, bulk, L);
@@ -311,13 +349,7 @@ int plan_gather(const GatherArgs& a0, int bank_dtype, int idx_dtype, int w_dtype
         *L = GatherLaunch{};
         return rc;
     }
-    int per_sm = 0;
-    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, L->fn, (int)L->block, L->smem);
-    if (e != cudaSuccess) {
-        (void)cudaGetLastError();
-        per_sm = 0;
-    }
-    L->early_trigger = blocks <= (int64_t)per_sm * sm_count() ? 1 : 0;
+    L->early_trigger = blocks <= (int64_t)blocks_per_sm(L->fn, (int)L->block, L->smem) * sm_count() ? 1 : 0;
     return 0;
 }
 

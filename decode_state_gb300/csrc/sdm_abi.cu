@@ -4,6 +4,8 @@
 #include <atomic>
 #include <climits>
 #include <cstring>
+#include <mutex>
+#include <vector>
 
 #include "sdm.h"
 #include "sdm_internal.h"
@@ -62,6 +64,63 @@ size_t smem_per_sm() {
 size_t smem_reserved_per_block() {
     static std::atomic<int> cache[64];
     return (size_t)device_attribute(cache, cudaDevAttrReservedSharedMemoryPerBlock, 1024);
+}
+
+int allow_smem(const void* kernel, size_t smem) {
+    if (smem <= 48 * 1024) return 0;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) {
+        (void)cudaGetLastError();
+        return (int)e;
+    }
+    struct Raised {
+        const void* fn;
+        int dev;
+        size_t bytes;
+    };
+    static std::mutex mu;
+    static std::vector<Raised> raised;  // one entry per (kernel, device) raised so far
+    std::lock_guard<std::mutex> lock(mu);
+    Raised* r = nullptr;
+    for (Raised& x : raised)
+        if (x.fn == kernel && x.dev == dev) r = &x;
+    if (r != nullptr && r->bytes >= smem) return 0;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) {
+        (void)cudaGetLastError();
+        return (int)e;
+    }
+    if (r != nullptr)
+        r->bytes = smem;
+    else
+        raised.push_back(Raised{kernel, dev, smem});
+    return 0;
+}
+
+int blocks_per_sm(const void* kernel, int threads, size_t smem) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return 0;
+    }
+    struct Entry {
+        const void* fn;
+        int dev, threads;
+        size_t smem;
+        int per_sm;
+    };
+    thread_local Entry cache[16] = {};
+    thread_local unsigned next = 0;
+    for (const Entry& x : cache)
+        if (x.fn == kernel && x.dev == dev && x.threads == threads && x.smem == smem) return x.per_sm;
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, smem) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return 0;
+    }
+    cache[next++ % 16] = Entry{kernel, dev, threads, smem, n};
+    return n;
 }
 
 }  // namespace sdm

@@ -37,12 +37,34 @@ __device__ __forceinline__ int64_t load_index(const void* p, int64_t i) {
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
+// ---------------------------------------------------------------- L2 eviction policy
+
+// A cache policy that marks every line it touches evict-first in L2: for output that this launch
+// never reads again (readings, stash rows, written-back rows that a later token rarely names).
+__device__ __forceinline__ uint64_t l2_evict_first() {
+    uint64_t p;
+    asm("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+// A 4-byte global store under an L2 cache policy.
+__device__ __forceinline__ void st_hint(float* p, float v, uint64_t pol) {
+    asm volatile("st.global.L2::cache_hint.b32 [%0], %1, %2;" ::"l"(p), "r"(__float_as_uint(v)), "l"(pol) : "memory");
+}
+
 // ---------------------------------------------------------------- bulk stores (async proxy)
 
 // shared -> global, tracked by the issuing thread's bulk groups.
 __device__ __forceinline__ void bulk_s2g(void* dst, const void* src, uint32_t bytes) {
     asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(smem_u32(src)),
                  "r"(bytes)
+                 : "memory");
+}
+
+// the same, with the destination lines marked by an L2 cache policy
+__device__ __forceinline__ void bulk_s2g_hint(void* dst, const void* src, uint32_t bytes, uint64_t pol) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group.L2::cache_hint [%0], [%1], %2, %3;" ::"l"(dst),
+                 "r"(smem_u32(src)), "r"(bytes), "l"(pol)
                  : "memory");
 }
 

@@ -77,13 +77,14 @@ size_t smem_reserved_per_block();
 
 // Let `kernel` use `smem` bytes of dynamic shared memory (raises the limit above the default 48 KB
 // on the current device). Called before any occupancy query of that launch, so that the query sees
-// the launch's real limit. Returns a cudaError_t.
-inline int allow_smem(const void* kernel, size_t smem) {
-    if (smem <= 48 * 1024) return 0;
-    const cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) (void)cudaGetLastError();
-    return (int)e;
-}
+// the launch's real limit. The limit only ever grows (to the largest size asked for so far per
+// kernel and device), so that concurrent callers cannot lower it under each other, and a kernel
+// whose limit already suffices costs no runtime call. Returns a cudaError_t.
+int allow_smem(const void* kernel, size_t smem);
+
+// Blocks of `kernel` resident per SM with `threads` threads and `smem` bytes of dynamic shared
+// memory on the current device (0 when the query fails), cached per host thread.
+int blocks_per_sm(const void* kernel, int threads, size_t smem);
 
 // Launch the kernel at address `kernel` (arguments as an array of pointers to them) with
 // programmatic stream serialization (see grid_dependency_wait). The dynamic shared-memory limit
@@ -123,12 +124,7 @@ int launch_pdl(void (*kernel)(P...), dim3 grid, dim3 block, size_t smem, cudaStr
 // scheduled early cannot take the place of blocks of this one.
 template <typename... P>
 bool fits_one_wave(void (*kernel)(P...), int64_t blocks, int threads, size_t smem) {
-    int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, smem) != cudaSuccess) {
-        (void)cudaGetLastError();
-        return false;
-    }
-    return blocks <= (int64_t)per_sm * sm_count();
+    return blocks <= (int64_t)blocks_per_sm(reinterpret_cast<const void*>(kernel), threads, smem) * sm_count();
 }
 
 }  // namespace sdm
