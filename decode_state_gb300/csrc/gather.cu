@@ -38,6 +38,7 @@ __device__ unsigned int g_gather_status;
 
 constexpr int kMaxThreads = 256;
 constexpr size_t kRowsBudget = 40 * 1024;
+constexpr int kFullSlice = 128;  // the slice width with its own kernel instance
 
 __host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -112,12 +113,15 @@ __device__ void write_padding(const GatherArgs& a, int64_t t, int op, int c0, in
     }
 }
 
-template <typename E, typename I, typename WT, bool BULK>
+// SW: the slice width in columns when it is known at compile time (the common full row of 128
+// columns: row addresses in shared memory become immediate offsets), 0 when it is taken from the
+// arguments.
+template <typename E, typename I, typename WT, bool BULK, int SW>
 __global__ void __launch_bounds__(kMaxThreads) gather_kernel(const GatherArgs a, int stash_bulk, int early_trigger) {
     constexpr int ES = sizeof(E);
     extern __shared__ __align__(128) unsigned char smem[];
 
-    const int hd = a.hd, sw = a.slice_cols;
+    const int hd = a.hd, sw = SW ? SW : a.slice_cols;
     const int W0 = a.width[0], W1 = a.n_ops == 2 ? a.width[1] : 0;
     // one block per (token, column slice, operand): operand op's NR entries
     const int op = (int)(blockIdx.x % a.n_ops);
@@ -287,7 +291,9 @@ __global__ void __launch_bounds__(kMaxThreads) gather_kernel(const GatherArgs a,
 
 template <typename E, typename I, typename WT>
 void resolve_typed(bool bulk, GatherLaunch* L) {
-    const auto kernel = bulk ? gather_kernel<E, I, WT, true> : gather_kernel<E, I, WT, false>;
+    const auto kernel = !bulk ? gather_kernel<E, I, WT, false, 0>
+                        : L->a.slice_cols == kFullSlice ? gather_kernel<E, I, WT, true, kFullSlice>
+                                                        : gather_kernel<E, I, WT, true, 0>;
     L->fn = reinterpret_cast<const void*>(kernel);
 }
 
