@@ -1387,7 +1387,7 @@ int launch_typed(int path, bool scalar, const DecodeArgs& a, dim3 grid, dim3 blo
 }
 
 constexpr int kWideRowsMin = 12;  // chunk rows of the float32 streaming kernel, at least
-constexpr int kWideRowsMax = 32;  // and at most
+constexpr int kWideRowsMax = 48;  // and at most
 
 // Geometry of decode_wide_kernel: one block per (stream, slice of up to 256 columns), a column per
 // thread. Each block is a chain of dependent row fetches whose time per token is set by the round
