@@ -630,15 +630,24 @@ def plan_slabs(dev, slab: int = 256) -> dict:
         for k in range(n):
             sdm.gather(g["bank"], slabs[k], chunk=wl.chunk, outs=outs, with_stash=False)
 
+    walk_rows, _ = sdm.GatherPlan.walk_arrays([k * slab for k in range(n)])
+
+    def native_walk():  # every slab from one call into the library's own loop
+        plan.walk(walk_rows)
+
+    def native_walk_ready():
+        plan.walk(walk_rows, inputs_ready=True)
+
     res = {"slab_tokens": slab, "launches_per_walk": n}
-    for name, fn in (("plan", via_plan), ("plan_ready", via_plan_ready), ("direct", direct)):
+    for name, fn in (("plan", via_plan), ("plan_ready", via_plan_ready), ("plan_walk", native_walk),
+                     ("plan_walk_ready", native_walk_ready), ("direct", direct)):
         ms = _time_calls(fn, 5)
         torch.cuda.synchronize()
         t0 = time.perf_counter()
         fn()
         host_us = (time.perf_counter() - t0) * 1e6 / n
         torch.cuda.synchronize()
-        res[name] = {"ms_per_walk": ms, "us_per_launch": ms * 1e3 / n, "host_us_per_call": host_us}
+        res[name] = {"ms_per_walk": ms, "us_per_launch": ms * 1e3 / n, "host_us_per_launch": host_us}
     # the plan walks replayed from CUDA graphs: device time per launch without the host calls
     side = torch.cuda.Stream(dev)
     for name, fn in (("plan_graph", via_plan), ("plan_ready_graph", via_plan_ready)):

@@ -364,28 +364,43 @@ int sdm_gather_plan_launch(const sdm_gather_plan* plan, int64_t row0, int valid,
 
 int sdm_gather_plan_launch_ex(const sdm_gather_plan* plan, int64_t row0, int valid, unsigned flags,
                               sdm_stream_t stream) {
+    const int32_t v = valid;
+    return sdm_gather_plan_walk(plan, &row0, &v, 1, flags, stream);
+}
+
+int sdm_gather_plan_walk(const sdm_gather_plan* plan, const int64_t* row0, const int32_t* valid, int n,
+                         unsigned flags, sdm_stream_t stream) {
     if (flags & ~SDM_INPUTS_READY) return SDM_EFLAGS;
-    if (!plan) return SDM_ENULL;
+    if (!plan || (n > 0 && !row0)) return SDM_ENULL;
+    if (n < 0) return SDM_ECOUNT;
     PlanRecord p;
     std::memcpy(&p, plan, sizeof(p));
     if (p.tag != plan_tag() || p.bytes != sizeof(PlanRecord)) return SDM_EPLAN;
-    if (row0 < 0 || row0 > p.row0_max) return SDM_EROW;
-    if (valid < 0 || valid > p.chunk) return SDM_ECHUNK;
-    if (p.launch.fn == nullptr) return SDM_OK;
+    for (int i = 0; i < n; ++i)
+        if (row0[i] < 0 || row0[i] > p.row0_max) return SDM_EROW;
+    if (valid)
+        for (int i = 0; i < n; ++i)
+            if (valid[i] < 0 || valid[i] > p.chunk) return SDM_ECHUNK;
+    if (p.launch.fn == nullptr || n == 0) return SDM_OK;
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess) {
         (void)cudaGetLastError();
         return SDM_EDEVICE;
     }
     if (dev != p.device) return SDM_EDEVICE;
+    const sdm::GatherArgs base = p.launch.a;
     sdm::GatherArgs& a = p.launch.a;
-    for (int o = 0; o < a.n_ops; ++o) {
-        a.idx[o] = static_cast<const unsigned char*>(a.idx[o]) + row0 * p.idx_row_bytes[o];
-        a.w[o] = static_cast<const unsigned char*>(a.w[o]) + row0 * p.w_row_bytes[o];
-    }
-    a.valid = valid;
     a.inputs_ready = (flags & SDM_INPUTS_READY) ? 1 : 0;
-    return sdm::run_gather(p.launch, reinterpret_cast<cudaStream_t>(stream));
+    for (int i = 0; i < n; ++i) {
+        for (int o = 0; o < a.n_ops; ++o) {
+            a.idx[o] = static_cast<const unsigned char*>(base.idx[o]) + row0[i] * p.idx_row_bytes[o];
+            a.w[o] = static_cast<const unsigned char*>(base.w[o]) + row0[i] * p.w_row_bytes[o];
+        }
+        a.valid = valid ? valid[i] : p.chunk;
+        const int rc = sdm::run_gather(p.launch, reinterpret_cast<cudaStream_t>(stream));
+        if (rc != 0) return rc;
+    }
+    return SDM_OK;
 }
 
 const char* sdm_status_string(int status) {

@@ -22,7 +22,8 @@ SDM_DEV_TIMEOUT, SDM_DEV_BAD_INDEX = 1, 2
 
 ENTRY_POINTS = ("sdm_decode_step", "sdm_decode_step_ex", "sdm_decode_seq", "sdm_decode_seq_ex", "sdm_gather",
                 "sdm_gather_kpos",
-                "sdm_gather_plan_init", "sdm_gather_plan_launch", "sdm_gather_plan_launch_ex", "sdm_status_string",
+                "sdm_gather_plan_init", "sdm_gather_plan_launch", "sdm_gather_plan_launch_ex", "sdm_gather_plan_walk",
+                "sdm_status_string",
                 "sdm_device_status", "sdm_version")
 SDM_INPUTS_READY = 1  # flag of the _ex calls: the inputs predate the kernel launched just before
 SDM_STREAM_MAJOR = 2  # flag of sdm_decode_seq_ex: per-token arrays are [S, T, .] instead of [T, S, .]
@@ -78,6 +79,8 @@ def library() -> ctypes.CDLL:
             lib.sdm_gather_plan_launch.restype = i32
             lib.sdm_gather_plan_launch_ex.argtypes = [vp, i64, i32, ctypes.c_uint, vp]
             lib.sdm_gather_plan_launch_ex.restype = i32
+            lib.sdm_gather_plan_walk.argtypes = [vp, vp, vp, i32, ctypes.c_uint, vp]
+            lib.sdm_gather_plan_walk.restype = i32
             lib.sdm_status_string.argtypes = [i32]
             lib.sdm_status_string.restype = ctypes.c_char_p
             lib.sdm_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint), i32]
@@ -386,6 +389,30 @@ class GatherPlan:
             rc = library().sdm_gather_plan_launch(self._record, row0, v, st)
             _check("sdm_gather_plan_launch", rc)
         return self.outs
+
+    def walk(self, row0s, valids=None, *, inputs_ready: bool = False, stream=None):
+        """Every slab of a walk from one foreign call (sdm_gather_plan_walk): slab i is
+        ``launch(row0s[i], valids[i])``, in order; ``outs`` holds the last slab's result.
+        ``row0s`` and ``valids`` are host integer sequences (``valids`` None: every slab full).
+        For a walk replayed many times, pass the arrays from ``walk_arrays`` to skip the
+        conversion."""
+        r, v = row0s, valids
+        if not (isinstance(r, ctypes.Array) and (v is None or isinstance(v, ctypes.Array))):
+            r, v = self.walk_arrays(row0s, valids)
+        n = len(r)
+        if v is not None and len(v) != n:
+            raise ValueError("row0s and valids must have the same length")
+        st = _stream_handle(stream, self.device)
+        rc = library().sdm_gather_plan_walk(self._record, r, v, n, SDM_INPUTS_READY if inputs_ready else 0, st)
+        _check("sdm_gather_plan_walk", rc)
+        return self.outs
+
+    @staticmethod
+    def walk_arrays(row0s, valids=None):
+        """Host arrays for ``walk``: (int64 row offsets, int32 valid counts or None)."""
+        r = (ctypes.c_int64 * len(row0s))(*row0s)
+        v = None if valids is None else (ctypes.c_int32 * len(valids))(*valids)
+        return r, v
 
 
 def device_status(clear: bool = True) -> int:

@@ -259,6 +259,23 @@ int sdm_gather_plan_launch(const sdm_gather_plan* plan, int64_t row0, int valid,
 int sdm_gather_plan_launch_ex(const sdm_gather_plan* plan, int64_t row0, int valid, unsigned flags,
                               sdm_stream_t stream);
 
+/*
+ * sdm_gather_plan_walk - n steps of a plan from one call: the native step loop over a walk of
+ * slabs (sparse-delta-memory 2.0.0, cuda/gather_cuda.py: `token_gather_dc_step` driven from a
+ * native loop), without a host-language call per slab.
+ *
+ *   row0[i]    host array of n slab offsets (each 0 <= row0[i] <= row0_max)
+ *   valid[i]   host array of n live-token counts per chunk (0..chunk), or NULL: chunk for every slab
+ *   n          slabs, >= 0
+ *   flags      0 or SDM_INPUTS_READY (applies to every slab; see sdm_gather_plan_launch_ex)
+ * Slab i is exactly sdm_gather_plan_launch_ex(plan, row0[i], valid[i], flags, stream), enqueued in
+ * order on `stream`. Every argument is checked before the first launch: an SDM_E* code means
+ * nothing was launched. A positive return is the cudaError_t of the first failed launch; the
+ * slabs before it were launched, none after it.
+ */
+int sdm_gather_plan_walk(const sdm_gather_plan* plan, const int64_t* row0, const int32_t* valid, int n,
+                         unsigned flags, sdm_stream_t stream);
+
 /* A static string naming a return code of the calls above. */
 const char* sdm_status_string(int status);
 

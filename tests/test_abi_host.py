@@ -221,6 +221,19 @@ def test_gather_plan_launch_ex_flags(lib):
     assert lib.sdm_gather_plan_launch_ex(zero, 0, 16, sdm.SDM_INPUTS_READY, None) == CODES["SDM_EPLAN"]
 
 
+def test_gather_plan_walk_argument_errors(lib):
+    """The walk refuses unknown flags, a NULL record or row list, a negative count and a foreign
+    record before launching anything."""
+    zero = ctypes.create_string_buffer(sdm.GATHER_PLAN_BYTES)
+    rows = (ctypes.c_int64 * 2)(0, 1)
+    assert lib.sdm_gather_plan_walk(zero, rows, None, 2, 4, None) == CODES["SDM_EFLAGS"]
+    assert lib.sdm_gather_plan_walk(None, rows, None, 2, 0, None) == CODES["SDM_ENULL"]
+    assert lib.sdm_gather_plan_walk(zero, None, None, 2, 0, None) == CODES["SDM_ENULL"]
+    assert lib.sdm_gather_plan_walk(zero, rows, None, -1, 0, None) == CODES["SDM_ECOUNT"]
+    assert lib.sdm_gather_plan_walk(zero, rows, None, 2, sdm.SDM_INPUTS_READY, None) == CODES["SDM_EPLAN"]
+    assert lib.sdm_gather_plan_walk(zero, None, None, 0, 0, None) == CODES["SDM_EPLAN"]
+
+
 def test_gather_plan_launch_refuses_a_foreign_record(lib):
     zero = ctypes.create_string_buffer(sdm.GATHER_PLAN_BYTES)
     assert lib.sdm_gather_plan_launch(zero, 0, 16, None) == CODES["SDM_EPLAN"]

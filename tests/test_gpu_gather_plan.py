@@ -153,3 +153,41 @@ def test_flagged_launches_after_decode_steps_see_their_writes():
     assert bits_equal(to_np(bank_p), to_np(bank_f))
     for a, b in zip(plain, flagged):
         assert bits_equal(to_np(a[0]), to_np(b[0])) and bits_equal(to_np(a[1]), to_np(b[1]))
+
+
+def test_plan_walk_applies_each_slab():
+    """sdm_gather_plan_walk: slab i of a walk is launch(row0[i], valid[i]); the outputs hold the last
+    slab's gather, for walks ending at every slab of the list (and with inputs_ready)."""
+    g = _inputs("bf16", "bf16", "i64", 5000, 128, 320, (64, 64), seed=21)
+    tokens, chunk = 64, 16
+    plan = sdm.GatherPlan(g["bank"], g["ops"], tokens=tokens, chunk=chunk)
+    row0s, valids = [0, 200, 37, 256, 5], [16, 3, 0, 16, 11]
+    for end in range(1, len(row0s) + 1):
+        for ready in (False, True):
+            for o in plan.outs:
+                o.fill_(float("nan"))
+            outs = plan.walk(row0s[:end], valids[:end], inputs_ready=ready)
+            torch.cuda.synchronize()
+            ref = _slab_oracle(g, row0s[end - 1], tokens, chunk, valids[end - 1])
+            for o in range(2):
+                assert bits_equal(to_np(outs[o]), ref[o]), (end, ready, o)
+    outs = plan.walk([7, 96])  # valid omitted: every slab full
+    torch.cuda.synchronize()
+    ref = _slab_oracle(g, 96, tokens, chunk, chunk)
+    assert bits_equal(to_np(outs[0]), ref[0]) and bits_equal(to_np(outs[1]), ref[1])
+
+
+def test_plan_walk_checks_every_slab_before_launching():
+    g = _inputs("f32", "f32", "i64", 500, 64, 40, (8,), seed=4)
+    plan = sdm.GatherPlan(g["bank"], g["ops"], tokens=16, chunk=8, row0_max=20)
+    plan.outs[0].fill_(float("nan"))
+    torch.cuda.synchronize()
+    for row0s, valids, code in (([0, 8, 21], None, EROW), ([0, 4], [8, 9], ECHUNK), ([3, -1], [1, 1], EROW)):
+        with pytest.raises(sdm.SDMError) as e:
+            plan.walk(row0s, valids)
+        assert e.value.status == code
+    torch.cuda.synchronize()
+    assert torch.isnan(plan.outs[0]).all()  # no slab of a refused walk was launched
+    plan.walk([], [])  # an empty walk launches nothing
+    torch.cuda.synchronize()
+    assert torch.isnan(plan.outs[0]).all()
