@@ -64,3 +64,22 @@ def test_gather_on_a_misaligned_bank_and_stash():
                                chunk_valid=to_np(g["chunk_valid"]))
     assert bits_equal(to_np(outs[0]), r0) and bits_equal(to_np(outs[1]), r1)
     assert bits_equal(to_np(stash), rs)
+
+
+@pytest.mark.parametrize("wdt", ["bf16", "f32"])
+def test_gather_aligned_bank_misaligned_stash_and_outputs(wdt):
+    """An aligned bank keeps the 16-byte row copies (and the 128-column instance) while the stash and
+    the outputs start off a 16-byte boundary: the stash leaves shared memory column by column
+    instead of as one bulk store, and padding tokens zero it the same way."""
+    wl = workloads.GatherWorkload("misaligned_stash", "bf16", 900, 128, 48, 16, (20, 9), "i64", wdt, 0.125, seed=23)
+    g = workloads.make_gather_inputs(wl, device=DEV)
+    stash = _shifted(torch.full((wl.tokens, wl.widths[0], wl.hd), 3.0, dtype=g["bank"].dtype, device=DEV))
+    outs = [_shifted(torch.full((wl.tokens, wl.hd), 5.0, device=DEV)) for _ in range(2)]
+    assert g["bank"].data_ptr() % 16 == 0
+    sdm.gather(g["bank"], g["ops"], chunk=wl.chunk, chunk_valid=g["chunk_valid"], stash=stash, outs=outs)
+    torch.cuda.synchronize()
+    (i0, w0), (i1, w1) = g["ops"]
+    r0, r1, rs = oracle.gather(to_np(g["bank"]), to_np(i0), to_np(w0), to_np(i1), to_np(w1), chunk=wl.chunk,
+                               chunk_valid=to_np(g["chunk_valid"]))
+    assert bits_equal(to_np(outs[0]), r0) and bits_equal(to_np(outs[1]), r1)
+    assert bits_equal(to_np(stash), rs)
