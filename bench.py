@@ -230,13 +230,14 @@ def oracle_gather_tokens(bank_h, g: dict, tokens, chunk: int):
     return len(tokens), time.perf_counter() - t0
 
 
-def decode_config(wl, r: sdist.Rank, call: str) -> dict:
+def decode_config(wl, r: sdist.Rank) -> dict:
     """The config object of a decode workload's JSON line (wl: one rank's share); both arms use
-    it, so that they name the same workload with the same keys (only `call` differs)."""
+    it, so that they name the same workload with the same keys and values (the entry point each
+    arm calls is the line's own `call` key)."""
     bank_gib = wl.n_slots * wl.hd * (2 if wl.bank_dtype == "bf16" else 4) / 2 ** 30
     return {"workload": wl.name, "streams": wl.n_streams, "head_dim": wl.hd,
             "slots_per_stream": wl.slots_per_stream, "W": wl.W, "R": wl.R, "G": wl.G, "T": wl.T,
-            "bank_dtype": wl.bank_dtype, "idx_dtype": wl.idx_dtype, "call": call,
+            "bank_dtype": wl.bank_dtype, "idx_dtype": wl.idx_dtype,
             "l2": (f"inputs larger than L2 ({bank_gib:.2f} GiB bank), no flush" if bank_gib > 0.2 else
                    f"L2-resident ({bank_gib * 1024:.0f} MiB bank)"),
             "parallelism": (f"weak: a job of {wl.n_streams * r.world} streams split into {r.world} contiguous "
@@ -324,11 +325,16 @@ class Case:
             return {"workload": wl.name, "n_slots": wl.n_slots, "head_dim": wl.hd, "tokens": wl.tokens,
                     "chunk": wl.chunk, "widths": list(wl.widths), "bank_dtype": wl.bank_dtype,
                     "idx_dtype": wl.idx_dtype, "w_dtype": wl.w_dtype, "stash": self.form == "stash",
-                    "form": self.form, "call": "sdm_gather_kpos" if self.form == "compact" else "sdm_gather",
+                    "form": self.form,
                     "l2": f"inputs larger than L2 ({gib:.0f} GiB bank), no flush", "parallelism": par}
-        call = {"decode_seq": "sdm_decode_seq", "decode_seq_stream_major": "sdm_decode_seq_ex (SDM_STREAM_MAJOR)",
+        return decode_config(wl, r)
+
+    def call(self) -> str:
+        """The library entry point the timed step calls."""
+        if self.kind == "gather":
+            return "sdm_gather_kpos" if self.form == "compact" else "sdm_gather"
+        return {"decode_seq": "sdm_decode_seq", "decode_seq_stream_major": "sdm_decode_seq_ex (SDM_STREAM_MAJOR)",
                 "decode_step": "sdm_decode_step x T"}[self.kind]
-        return decode_config(wl, r, call)
 
     # end to end: host inputs in, results out, every step
     def e2e(self, steps: int, r: sdist.Rank) -> dict:
@@ -505,7 +511,7 @@ def run_ours(args, r: sdist.Rank):
     res = {
         "metric": case.metric, "value": value, "unit": case.unit, "n_gpus": r.world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": max_ms / args.steps, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f32", "data": "synthetic", "config": case.config(r),
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic", "config": case.config(r), "call": case.call(),
         "effective_gbs": case.nbytes * args.steps * r.world / (max_ms / 1e3) / 1e9,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": ncu_traffic(case.wl.name), "peak_kind": peak_kind, "kernel": case.kernel,
@@ -755,7 +761,7 @@ def run_reference(args, r: sdist.Rank):
     return {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": r.world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs * 1e3 / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-            "config": decode_config(base, r, "oracle_sdm_decode_seq"),
+            "config": decode_config(base, r), "call": "oracle_sdm_decode_seq (CPU)",
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
