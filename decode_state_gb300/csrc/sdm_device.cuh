@@ -52,6 +52,13 @@ __device__ __forceinline__ void st_hint(float* p, float v, uint64_t pol) {
     asm volatile("st.global.L2::cache_hint.b32 [%0], %1, %2;" ::"l"(p), "r"(__float_as_uint(v)), "l"(pol) : "memory");
 }
 
+// A 16-byte global store of four floats under an L2 cache policy.
+__device__ __forceinline__ void st_hint4(void* p, float a, float b, float c, float d, uint64_t pol) {
+    asm volatile("st.global.L2::cache_hint.v4.f32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(p), "f"(a), "f"(b), "f"(c),
+                 "f"(d), "l"(pol)
+                 : "memory");
+}
+
 // ---------------------------------------------------------------- bulk stores (async proxy)
 
 // shared -> global, tracked by the issuing thread's bulk groups.
