@@ -26,7 +26,7 @@
 //      owners publish their delta pairs and the write goes by 16-byte pieces instead (thread =
 //      row group and piece, one 16-byte load and store per row it takes), which needs a quarter
 //      of the per-row loads, stores and address work; otherwise each thread writes its own pair
-//      of every row;
+//      of every row (the one-column kernel for narrow slices always writes by pieces);
 //   3. a barrier, then the R read rows by 16-byte cp.async, and each thread reduces its columns
 //      over ascending r (for bf16 banks with the mixed-precision fma, whose bf16 operands need no
 //      widening); meanwhile the next token's write rows are prefetched into L2, so that its
@@ -45,7 +45,8 @@
 // Arithmetic per element (float32; every paired op is two independent round-to-nearest ops):
 //   a_w = kv_w * d_w;  retrieved = fma(a_w, row_w, .) over w;  delta = beta * (round(v) - retrieved)
 //   new_w = fma(kv_w, delta, row_w * d_w);  readings = fma(qv_r, row_r, .) over r
-// with d_w the float32 nearest to e^g (computed in double precision and rounded once).
+// with d_w the float32 nearest to e^g (gate(): a float32-pair table evaluation kept when a rounding
+// test proves it is that float32, the double-precision exponential rounded once otherwise).
 #include <algorithm>
 #include <climits>
 
