@@ -604,6 +604,10 @@ def extras(args, dev, r: sdist.Rank, peak: float, skip: str):
             rms = _time_calls(plan_steps, reps)
             item.update({"plan_ready_unit_per_s": case.units / (rms / 1e3), "plan_ready_ms_per_step": rms,
                          "plan_ready_us_per_launch": rms * 1e3 / case.launches})
+            # every step of the plan from one call into the library's own loop (sdm_decode_plan_walk)
+            wms = _time_calls(plan.walk, reps)
+            item.update({"plan_walk_ready_unit_per_s": case.units / (wms / 1e3), "plan_walk_ready_ms_per_step": wms,
+                         "plan_walk_ready_us_per_launch": wms * 1e3 / case.launches})
             del plan
         res[name] = item
         del case

@@ -1398,7 +1398,7 @@ auto stream_kernel(int ns, int sw) {
 }
 
 template <typename E, typename I>
-int launch_typed(int path, bool scalar, const DecodeArgs& a, dim3 grid, dim3 block, size_t smem, cudaStream_t stream) {
+const void* resolve_kernel(int path, bool scalar, const DecodeArgs& a) {
     const auto kernel =
         path == kStaged
             ? ((sizeof(E) == 2 && scalar)
@@ -1406,10 +1406,7 @@ int launch_typed(int path, bool scalar, const DecodeArgs& a, dim3 grid, dim3 blo
                    : (a.piece_write ? vec_kernel<E, I, true>(a.slice_cols) : vec_kernel<E, I, false>(a.slice_cols)))
         : path == kStream ? stream_kernel<E, I>(a.stream_stages, a.slice_cols)
                           : decode_simt_kernel<E, I>;
-    const int rc = allow_smem(reinterpret_cast<const void*>(kernel), smem);  // before the occupancy query
-    if (rc != 0) return rc;
-    const int early = fits_one_wave(kernel, grid.x, (int)block.x, smem) ? 1 : 0;
-    return launch_pdl(kernel, grid, block, smem, stream, a, early);
+    return reinterpret_cast<const void*>(kernel);
 }
 
 constexpr int kWideRowsMin = 12;  // chunk rows of the float32 streaming kernel, at least
@@ -1472,7 +1469,23 @@ int shrink_cols(int sw, int q) {
 
 }  // namespace
 
-int launch_decode(const DecodeArgs& a0, int bank_dtype, int idx_dtype, cudaStream_t stream) {
+int launch_decode(const DecodeArgs& a, int bank_dtype, int idx_dtype, cudaStream_t stream) {
+    DecodeLaunch L;
+    const int rc = plan_decode(a, bank_dtype, idx_dtype, &L);
+    if (rc != 0) return rc;
+    return run_decode(L, stream);
+}
+
+int run_decode(const DecodeLaunch& L, cudaStream_t stream) {
+    if (L.fn == nullptr) return 0;
+    DecodeArgs a = L.a;
+    int early = L.early_trigger;
+    void* args[] = {&a, &early};
+    return launch_pdl_raw(L.fn, dim3(L.grid), dim3(L.block), L.smem, stream, args);
+}
+
+int plan_decode(const DecodeArgs& a0, int bank_dtype, int idx_dtype, DecodeLaunch* L) {
+    *L = DecodeLaunch{};
     DecodeArgs a = a0;
     if (a.n_streams == 0 || a.T == 0) return 0;
     const int es = bank_dtype == SDM_BF16 ? 2 : 4;
@@ -1579,13 +1592,22 @@ int launch_decode(const DecodeArgs& a0, int bank_dtype, int idx_dtype, cudaStrea
                                        : StreamLayout(a.W, a.R, a.G, sw, es, is, a.stream_rows, a.stream_stages).total)
                             : SimtLayout(a.W, a.R, sw, es).total;
 
-    const dim3 grid((unsigned)blocks_final), block((unsigned)threads);
-    if (bank_dtype == SDM_BF16) {
-        return idx_dtype == SDM_I32 ? launch_typed<uint16_t, int32_t>(path, scalar, a, grid, block, smem, stream)
-                                    : launch_typed<uint16_t, int64_t>(path, scalar, a, grid, block, smem, stream);
-    }
-    return idx_dtype == SDM_I32 ? launch_typed<float, int32_t>(path, scalar, a, grid, block, smem, stream)
-                                : launch_typed<float, int64_t>(path, scalar, a, grid, block, smem, stream);
+    const void* fn = bank_dtype == SDM_BF16
+                         ? (idx_dtype == SDM_I32 ? resolve_kernel<uint16_t, int32_t>(path, scalar, a)
+                                                 : resolve_kernel<uint16_t, int64_t>(path, scalar, a))
+                         : (idx_dtype == SDM_I32 ? resolve_kernel<float, int32_t>(path, scalar, a)
+                                                 : resolve_kernel<float, int64_t>(path, scalar, a));
+    const int rc = allow_smem(fn, smem);  // before the occupancy query
+    if (rc != 0) return rc;
+    // the early trigger only when every block of this launch is resident at once, so that blocks
+    // of the next kernel scheduled early cannot take the place of blocks of this one
+    L->early_trigger = blocks_final <= (int64_t)blocks_per_sm(fn, threads, smem) * sm_count() ? 1 : 0;
+    L->fn = fn;
+    L->a = a;
+    L->grid = (unsigned)blocks_final;
+    L->block = (unsigned)threads;
+    L->smem = smem;
+    return 0;
 }
 
 int decode_status(unsigned int* word, bool clear) {

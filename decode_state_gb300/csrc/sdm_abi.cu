@@ -303,9 +303,112 @@ uint64_t plan_tag() {
     return 0x4e414c5047534453ull ^ (uint64_t)reinterpret_cast<uintptr_t>(&check_gather);
 }
 
+// The contents of an sdm_decode_plan record: the launch of token 0 and the byte step of every
+// per-token array from one token to the next (time-major: n_streams rows per token).
+struct DecodePlanRecord {
+    uint64_t tag;
+    uint64_t bytes;
+    int64_t step[8];  // k_idx, k_val, v, beta, g, q_idx, q_val, out
+    int32_t device, T;
+    sdm::DecodeLaunch launch;  // token 0; nullptr kernel: nothing to launch
+};
+static_assert(sizeof(DecodePlanRecord) <= SDM_DECODE_PLAN_BYTES, "decode plan record too large");
+
+uint64_t decode_plan_tag() {
+    return 0x4e414c50434544ull ^ (uint64_t)reinterpret_cast<uintptr_t>(&check_decode);
+}
+
 }  // namespace
 
 extern "C" {
+
+int sdm_decode_plan_init(sdm_decode_plan* plan, void* bank, const void* k_idx, const float* k_val, const float* v,
+                         const float* beta, const float* g, const void* q_idx, const float* q_val, void* out,
+                         int64_t n_streams, int hd, int W, int R, int G, int T, int bank_dtype, int idx_dtype) {
+    if (!plan) return SDM_ENULL;
+    const int rc = check_decode(bank, k_idx, k_val, v, beta, g, q_idx, q_val, out, n_streams, hd, W, R, G, T,
+                                bank_dtype, idx_dtype);
+    if (rc != SDM_OK) return rc;
+    DecodePlanRecord p{};
+    const int64_t is = idx_dtype == SDM_I64 ? 8 : 4, es = bank_dtype == SDM_BF16 ? 2 : 4;
+    const int64_t per[8] = {W * is, W * 4, (int64_t)hd * 4, 4, (int64_t)G * 4, R * is, R * 4, (int64_t)hd * es};
+    for (int k = 0; k < 8; ++k) p.step[k] = per[k] * n_streams;
+    p.T = T;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) {
+        (void)cudaGetLastError();
+        return (int)e;
+    }
+    p.device = dev;
+    if (n_streams > 0 && T > 0) {
+        sdm::DecodeArgs a{};
+        a.bank = bank;
+        a.k_idx = k_idx;
+        a.k_val = k_val;
+        a.v = v;
+        a.beta = beta;
+        a.g = g;
+        a.q_idx = q_idx;
+        a.q_val = q_val;
+        a.out = out;
+        a.n_streams = n_streams;
+        a.hd = hd;
+        a.W = W;
+        a.R = R;
+        a.G = G;
+        a.T = 1;
+        a.tstride = n_streams;
+        a.sstride = 1;
+        const int lrc = sdm::plan_decode(a, bank_dtype, idx_dtype, &p.launch);
+        if (lrc != 0) return lrc;
+    }
+    p.tag = decode_plan_tag();
+    p.bytes = sizeof(DecodePlanRecord);
+    static_assert(sizeof(sdm_decode_plan) == SDM_DECODE_PLAN_BYTES, "decode plan record size");
+    std::memset(plan, 0, sizeof(sdm_decode_plan));
+    std::memcpy(plan, &p, sizeof(p));
+    return SDM_OK;
+}
+
+int sdm_decode_plan_launch(const sdm_decode_plan* plan, int t, unsigned flags, sdm_stream_t stream) {
+    return sdm_decode_plan_walk(plan, t, 1, flags, stream);
+}
+
+int sdm_decode_plan_walk(const sdm_decode_plan* plan, int t0, int n, unsigned flags, sdm_stream_t stream) {
+    if (flags & ~SDM_INPUTS_READY) return SDM_EFLAGS;
+    if (!plan) return SDM_ENULL;
+    if (n < 0) return SDM_ECOUNT;
+    DecodePlanRecord p;
+    std::memcpy(&p, plan, sizeof(p));
+    if (p.tag != decode_plan_tag() || p.bytes != sizeof(DecodePlanRecord)) return SDM_EPLAN;
+    if (n > 0 && (t0 < 0 || (int64_t)t0 + n > p.T)) return SDM_EROW;
+    if (p.launch.fn == nullptr || n == 0) return SDM_OK;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return SDM_EDEVICE;
+    }
+    if (dev != p.device) return SDM_EDEVICE;
+    const sdm::DecodeArgs base = p.launch.a;
+    sdm::DecodeArgs& a = p.launch.a;
+    a.inputs_ready = (flags & SDM_INPUTS_READY) ? 1 : 0;
+    const auto at = [](const void* q, int64_t off) { return static_cast<const unsigned char*>(q) + off; };
+    for (int i = 0; i < n; ++i) {
+        const int64_t t = (int64_t)t0 + i;
+        a.k_idx = at(base.k_idx, t * p.step[0]);
+        a.k_val = reinterpret_cast<const float*>(at(base.k_val, t * p.step[1]));
+        a.v = reinterpret_cast<const float*>(at(base.v, t * p.step[2]));
+        a.beta = reinterpret_cast<const float*>(at(base.beta, t * p.step[3]));
+        a.g = reinterpret_cast<const float*>(at(base.g, t * p.step[4]));
+        a.q_idx = at(base.q_idx, t * p.step[5]);
+        a.q_val = reinterpret_cast<const float*>(at(base.q_val, t * p.step[6]));
+        a.out = static_cast<unsigned char*>(base.out) + t * p.step[7];
+        const int rc = sdm::run_decode(p.launch, reinterpret_cast<cudaStream_t>(stream));
+        if (rc != 0) return rc;
+    }
+    return SDM_OK;
+}
 
 int sdm_gather(const void* bank, int64_t n_slots, int hd, int bank_dtype, int n_ops, const void* const idx[2],
                const void* const w[2], float* const out[2], const int width[2], int idx_dtype, int w_dtype,
@@ -417,9 +520,9 @@ const char* sdm_status_string(int status) {
         case SDM_EALIGN: return "a pointer is not aligned to its element size";
         case SDM_EOVERLAP: return "a gather output or the stash overlaps the bank";
         case SDM_ENOPS: return "the gather takes one or two operands";
-        case SDM_EPLAN: return "not a gather plan made by sdm_gather_plan_init in this process";
-        case SDM_EROW: return "row0 outside 0..row0_max, or row0_max + tokens beyond the index rows";
-        case SDM_EDEVICE: return "the current device is not the gather plan's device";
+        case SDM_EPLAN: return "not a plan made by sdm_gather_plan_init / sdm_decode_plan_init in this process";
+        case SDM_EROW: return "row0 outside 0..row0_max, row0_max + tokens beyond the index rows, or a plan step outside 0..T-1";
+        case SDM_EDEVICE: return "the current device is not the plan's device";
         case SDM_EFLAGS: return "unknown bits in the flags of an _ex entry point";
         default: break;
     }

@@ -57,8 +57,20 @@ struct GatherLaunch {
     size_t smem;
 };
 
+// A resolved decode launch: the kernel instance, its geometry and every kernel argument.
+struct DecodeLaunch {
+    const void* fn;  // kernel (host stub of the template instance); nullptr: nothing to launch
+    DecodeArgs a;
+    int early_trigger;
+    unsigned int grid, block;
+    size_t smem;
+};
+
 // Validated launches (arguments already checked by the ABI layer). Return a cudaError_t.
 int launch_decode(const DecodeArgs& a, int bank_dtype, int idx_dtype, cudaStream_t stream);
+// launch_decode in two halves: choose the kernel and geometry (device queries, no launch), then launch.
+int plan_decode(const DecodeArgs& a, int bank_dtype, int idx_dtype, DecodeLaunch* L);
+int run_decode(const DecodeLaunch& L, cudaStream_t stream);
 int launch_gather(const GatherArgs& a, int bank_dtype, int idx_dtype, int w_dtype, cudaStream_t stream);
 // launch_gather in two halves: choose the kernel and geometry (device queries, no launch), then launch.
 int plan_gather(const GatherArgs& a, int bank_dtype, int idx_dtype, int w_dtype, GatherLaunch* L);
@@ -105,26 +117,6 @@ inline int launch_pdl_raw(const void* kernel, dim3 grid, dim3 block, size_t smem
     const cudaError_t e = cudaLaunchKernelExC(&cfg, kernel, args);
     if (e != cudaSuccess) (void)cudaGetLastError();
     return (int)e;
-}
-
-template <typename T>
-struct Same {
-    using type = T;
-};
-
-// launch_pdl_raw for a typed kernel; the arguments are converted to the kernel's parameter types.
-template <typename... P>
-int launch_pdl(void (*kernel)(P...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
-               typename Same<P>::type... args) {
-    void* argv[] = {&args...};
-    return launch_pdl_raw(reinterpret_cast<const void*>(kernel), grid, block, smem, stream, argv);
-}
-
-// True when all `blocks` of `kernel` can be resident at once, so that blocks of the next kernel
-// scheduled early cannot take the place of blocks of this one.
-template <typename... P>
-bool fits_one_wave(void (*kernel)(P...), int64_t blocks, int threads, size_t smem) {
-    return blocks <= (int64_t)blocks_per_sm(reinterpret_cast<const void*>(kernel), threads, smem) * sm_count();
 }
 
 }  // namespace sdm

@@ -20,7 +20,8 @@ SDM_BF16, SDM_F32 = 0, 1
 SDM_I32, SDM_I64 = 0, 1
 SDM_DEV_TIMEOUT, SDM_DEV_BAD_INDEX = 1, 2
 
-ENTRY_POINTS = ("sdm_decode_step", "sdm_decode_step_ex", "sdm_decode_seq", "sdm_decode_seq_ex", "sdm_gather",
+ENTRY_POINTS = ("sdm_decode_step", "sdm_decode_step_ex", "sdm_decode_seq", "sdm_decode_seq_ex",
+                "sdm_decode_plan_init", "sdm_decode_plan_launch", "sdm_decode_plan_walk", "sdm_gather",
                 "sdm_gather_kpos",
                 "sdm_gather_plan_init", "sdm_gather_plan_launch", "sdm_gather_plan_launch_ex", "sdm_gather_plan_walk",
                 "sdm_status_string",
@@ -28,6 +29,7 @@ ENTRY_POINTS = ("sdm_decode_step", "sdm_decode_step_ex", "sdm_decode_seq", "sdm_
 SDM_INPUTS_READY = 1  # flag of the _ex calls: the inputs predate the kernel launched just before
 SDM_STREAM_MAJOR = 2  # flag of sdm_decode_seq_ex: per-token arrays are [S, T, .] instead of [T, S, .]
 GATHER_PLAN_BYTES = 512  # SDM_GATHER_PLAN_BYTES
+DECODE_PLAN_BYTES = 512  # SDM_DECODE_PLAN_BYTES
 
 _BANK_CODES = {torch.bfloat16: SDM_BF16, torch.float32: SDM_F32}
 _IDX_CODES = {torch.int32: SDM_I32, torch.int64: SDM_I64}
@@ -65,6 +67,12 @@ def library() -> ctypes.CDLL:
             lib.sdm_decode_seq.restype = i32
             lib.sdm_decode_seq_ex.argtypes = dec + [i32, i32, i32, ctypes.c_uint, vp]
             lib.sdm_decode_seq_ex.restype = i32
+            lib.sdm_decode_plan_init.argtypes = [vp] + dec + [i32, i32, i32]
+            lib.sdm_decode_plan_init.restype = i32
+            lib.sdm_decode_plan_launch.argtypes = [vp, i32, ctypes.c_uint, vp]
+            lib.sdm_decode_plan_launch.restype = i32
+            lib.sdm_decode_plan_walk.argtypes = [vp, i32, i32, ctypes.c_uint, vp]
+            lib.sdm_decode_plan_walk.restype = i32
             lib.sdm_gather.argtypes = [vp, i64, i32, i32, i32, ctypes.POINTER(vp), ctypes.POINTER(vp),
                                        ctypes.POINTER(vp), ctypes.POINTER(i32), i32, i32, vp, i64, i32, i32, vp, vp]
             lib.sdm_gather.restype = i32
@@ -282,16 +290,17 @@ def gather(bank, ops, *, chunk: int, valid: int | None = None, chunk_valid=None,
 
 
 class DecodeStepPlan:
-    """Single-token decode steps over fixed device buffers, checked once (sdm_decode_step).
+    """Single-token decode steps over fixed device buffers, checked once (sdm_decode_plan_init).
 
     ``inputs`` maps the names of ``DECODE_KEYS`` to time-major device tensors [T, S, .] (beta
     [T, S]) that the caller fills; ``launch(t)`` runs sdm_decode_step on step t's slabs and writes
-    the readings into ``out[t]`` ([T, S, hd], allocated when not given). Shapes, dtypes, devices
-    and every step's pointers are settled here, so a launch is one foreign call. The plan keeps
+    the readings into ``out[t]`` ([T, S, hd], allocated when not given); ``walk(t0, n)`` runs steps
+    t0 .. t0 + n - 1 from one foreign call. Shapes, dtypes, devices and the launch are settled in a
+    plan record made here, so a launch is one foreign call with four arguments. The plan keeps
     references to its tensors; they must not be resized or reallocated in place.
 
-    With ``inputs_ready`` every launch passes SDM_INPUTS_READY (sdm_decode_step_ex): the caller
-    fills all T slabs before the launches, not between them.
+    With ``inputs_ready`` every launch passes SDM_INPUTS_READY: the caller fills all T slabs before
+    the launches, not between them.
     """
 
     DECODE_KEYS = ("k_idx", "k_val", "v", "beta", "g", "q_idx", "q_val")
@@ -303,12 +312,13 @@ class DecodeStepPlan:
         args = [inputs[k] for k in self.DECODE_KEYS]
         self.out, _, hd, W, R, G, _ = _decode_args(bank, *args, out, (T, inputs["k_idx"].shape[1]), stream)
         S = inputs["k_idx"].shape[1]
-        self._tail = (S, hd, W, R, G, _BANK_CODES[bank.dtype], _IDX_CODES[inputs["k_idx"].dtype])
-        if inputs_ready:
-            self._tail += (SDM_INPUTS_READY,)
-        self._steps = [(bank.data_ptr(), *(a[t].data_ptr() for a in args), self.out[t].data_ptr()) for t in range(T)]
-        self._name = "sdm_decode_step_ex" if inputs_ready else "sdm_decode_step"
-        self._fn = getattr(library(), self._name)
+        self._record = ctypes.create_string_buffer(DECODE_PLAN_BYTES)
+        rc = library().sdm_decode_plan_init(self._record, bank.data_ptr(), *(a.data_ptr() for a in args),
+                                            self.out.data_ptr(), S, hd, W, R, G, T, _BANK_CODES[bank.dtype],
+                                            _IDX_CODES[inputs["k_idx"].dtype])
+        _check("sdm_decode_plan_init", rc)
+        self._flags = SDM_INPUTS_READY if inputs_ready else 0
+        self._launch = library().sdm_decode_plan_launch
         self._stream = _stream_handle(stream, bank.device) if stream is not None else None
         self._keep = (bank, inputs)
         self.device, self.T = bank.device, T
@@ -316,10 +326,18 @@ class DecodeStepPlan:
     def launch(self, t: int, stream=None) -> torch.Tensor:
         """Step t (0 <= t < T) on the bank; returns the readings out[t]."""
         st = self._stream if stream is None and self._stream is not None else _stream_handle(stream, self.device)
-        rc = self._fn(*self._steps[t], *self._tail, st)
+        rc = self._launch(self._record, t, self._flags, st)
         if rc != 0:
-            _check(self._name, rc)
+            _check("sdm_decode_plan_launch", rc)
         return self.out[t]
+
+    def walk(self, t0: int = 0, n: int | None = None, stream=None) -> torch.Tensor:
+        """Steps t0 .. t0 + n - 1 (n: all the rest when None) from one call; returns ``out``."""
+        n = self.T - t0 if n is None else n
+        st = self._stream if stream is None and self._stream is not None else _stream_handle(stream, self.device)
+        rc = library().sdm_decode_plan_walk(self._record, t0, n, self._flags, st)
+        _check("sdm_decode_plan_walk", rc)
+        return self.out
 
 
 class GatherPlan:

@@ -67,9 +67,9 @@ typedef struct CUstream_st* sdm_stream_t;
 #define SDM_EALIGN (-9)     /* a pointer is not aligned to its element size */
 #define SDM_EOVERLAP (-10)  /* a gather output or the stash overlaps the bank */
 #define SDM_ENOPS (-11)     /* gather operand count is not 1 or 2 */
-#define SDM_EPLAN (-12)     /* not an initialised gather plan (wrong tag or record size) */
-#define SDM_EROW (-13)      /* row0 outside 0..row0_max, or row0_max + tokens beyond the index rows */
-#define SDM_EDEVICE (-14)   /* the current device is not the one the gather plan was made on */
+#define SDM_EPLAN (-12)     /* not an initialised gather or decode plan (wrong tag or record size) */
+#define SDM_EROW (-13)      /* row0 outside 0..row0_max, row0_max + tokens beyond the index rows, or a plan step outside 0..T-1 */
+#define SDM_EDEVICE (-14)   /* the current device is not the one the plan was made on */
 #define SDM_EFLAGS (-15)    /* unknown bits in the flags of an _ex entry point */
 
 /* bits of the device status word */
@@ -154,6 +154,46 @@ int sdm_decode_seq(void* bank, const void* k_idx, const float* k_val, const floa
 int sdm_decode_seq_ex(void* bank, const void* k_idx, const float* k_val, const float* v, const float* beta,
                       const float* g, const void* q_idx, const float* q_val, void* out, int64_t n_streams, int hd,
                       int W, int R, int G, int T, int bank_dtype, int idx_dtype, unsigned flags, sdm_stream_t stream);
+
+/*
+ * Decode-step plan: T single-token steps over time-major inputs, checked once (the decode-side
+ * counterpart of the gather launch plan below, for a loop that launches one token at a time, e.g.
+ * while serving). sdm_decode_plan_init checks the arguments of sdm_decode_seq(..., T, ...) once
+ * and records the launch of one token; sdm_decode_plan_launch(t) then launches exactly
+ * sdm_decode_step on the rows of token t (k_idx + t * n_streams * W, ..., out + t * n_streams * hd),
+ * and sdm_decode_plan_walk launches tokens t0 .. t0 + n - 1 in order from one call. The record is
+ * caller-owned, valid on the device current at init, in this process, until the library is
+ * unloaded; it keeps the pointers given at init (their memory must stay allocated). Every step
+ * returns 0, an SDM_E* code (nothing launched) or the cudaError_t of a failed launch.
+ */
+#define SDM_DECODE_PLAN_BYTES 512
+typedef struct sdm_decode_plan {
+    uint64_t opaque[SDM_DECODE_PLAN_BYTES / 8];
+} sdm_decode_plan;
+
+/*
+ * sdm_decode_plan_init - check a time-major T-token decode once and record a one-token launch in
+ * *plan (nothing is launched). Arguments as sdm_decode_seq; T >= 0. Returns 0, an SDM_E* code
+ * (the record untouched) or a cudaError_t from the device queries and settings.
+ */
+int sdm_decode_plan_init(sdm_decode_plan* plan, void* bank, const void* k_idx, const float* k_val, const float* v,
+                         const float* beta, const float* g, const void* q_idx, const float* q_val, void* out,
+                         int64_t n_streams, int hd, int W, int R, int G, int T, int bank_dtype, int idx_dtype);
+
+/*
+ * sdm_decode_plan_launch - step t of a plan (0 <= t < T, else SDM_EROW); flags 0 or
+ * SDM_INPUTS_READY (as for sdm_decode_step_ex). Checks, in order: the flags (SDM_EFLAGS), the
+ * record (SDM_EPLAN), t (SDM_EROW), the current device (SDM_EDEVICE).
+ */
+int sdm_decode_plan_launch(const sdm_decode_plan* plan, int t, unsigned flags, sdm_stream_t stream);
+
+/*
+ * sdm_decode_plan_walk - steps t0, t0 + 1, ..., t0 + n - 1 of a plan, enqueued in order from one
+ * call (n >= 0, else SDM_ECOUNT; every step inside 0..T-1, else SDM_EROW). All checks come before
+ * the first launch; a positive return is the cudaError_t of the first failed launch (the steps
+ * before it were launched, none after it).
+ */
+int sdm_decode_plan_walk(const sdm_decode_plan* plan, int t0, int n, unsigned flags, sdm_stream_t stream);
 
 /*
  * sdm_gather - token gather (gather_cuda.py, module docstring and token_gather).

@@ -221,6 +221,27 @@ def test_gather_plan_launch_ex_flags(lib):
     assert lib.sdm_gather_plan_launch_ex(zero, 0, 16, sdm.SDM_INPUTS_READY, None) == CODES["SDM_EPLAN"]
 
 
+def test_decode_plan_argument_errors(lib):
+    """The decode-step plan refuses unknown flags, a NULL record, a negative count and a foreign
+    record before launching anything; init checks its arguments like sdm_decode_seq."""
+    zero = ctypes.create_string_buffer(sdm.DECODE_PLAN_BYTES)
+    assert lib.sdm_decode_plan_walk(zero, 0, 1, 4, None) == CODES["SDM_EFLAGS"]
+    assert lib.sdm_decode_plan_launch(zero, 0, 2, None) == CODES["SDM_EFLAGS"]
+    assert lib.sdm_decode_plan_walk(None, 0, 1, 0, None) == CODES["SDM_ENULL"]
+    assert lib.sdm_decode_plan_walk(zero, 0, -1, 0, None) == CODES["SDM_ECOUNT"]
+    assert lib.sdm_decode_plan_walk(zero, 0, 1, sdm.SDM_INPUTS_READY, None) == CODES["SDM_EPLAN"]
+    assert lib.sdm_decode_plan_launch(zero, 0, 0, None) == CODES["SDM_EPLAN"]
+    junk = ctypes.create_string_buffer(bytes(range(256)) * 2)
+    assert lib.sdm_decode_plan_launch(junk, 0, 0, None) == CODES["SDM_EPLAN"]
+    record = ctypes.create_string_buffer(sdm.DECODE_PLAN_BYTES)
+    p = [FAKE] * 9
+    assert lib.sdm_decode_plan_init(None, *p, 4, 64, 8, 8, 1, 2, 0, 0) == CODES["SDM_ENULL"]
+    assert lib.sdm_decode_plan_init(record, *p, 4, 64, 8, 8, 3, 2, 0, 0) == CODES["SDM_EGATES"]
+    assert lib.sdm_decode_plan_init(record, *p, 4, 64, 0, 8, 1, 2, 0, 0) == CODES["SDM_EWIDTH"]
+    assert lib.sdm_decode_plan_init(record, *p, 4, 64, 8, 8, 1, 2, 7, 0) == CODES["SDM_EDTYPE"]
+    assert record.raw == bytes(sdm.DECODE_PLAN_BYTES)  # nothing written on an error
+
+
 def test_gather_plan_walk_argument_errors(lib):
     """The walk refuses unknown flags, a NULL record or row list, a negative count and a foreign
     record before launching anything."""

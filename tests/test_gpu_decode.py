@@ -245,6 +245,43 @@ def test_decode_step_plan_matches_eager_steps():
     assert torch.equal(bank_p.view(torch.int32), x["bank"].view(torch.int32))
 
 
+@pytest.mark.parametrize("case", [SMALL[1], SMALL[5], SMALL[8]], ids=[IDS[1], IDS[5], IDS[8]])
+def test_decode_plan_walk_matches_seq_and_oracle(case):
+    """sdm_decode_plan_walk: a walk over all T steps (in two parts, one with SDM_INPUTS_READY)
+    gives the bits of one sdm_decode_seq launch and of the oracle, on the staged, narrow-slice and
+    streamed kernels."""
+    wl = _wl(*case)
+    x = workloads.make_decode_inputs(wl, device=DEV)
+    bank_ref, out_ref = _oracle_seq(x)
+    bank_s = x["bank"].clone()
+    out_s = sdm.decode_seq(bank_s, *(x[k] for k in DECODE_KEYS))
+    plan = sdm.DecodeStepPlan(x["bank"], {k: x[k] for k in DECODE_KEYS})
+    plan.walk(0, 1)
+    ready = sdm.DecodeStepPlan(x["bank"], {k: x[k] for k in DECODE_KEYS}, out=plan.out, inputs_ready=True)
+    ready.walk(1)
+    torch.cuda.synchronize()
+    assert bits_equal(to_np(plan.out), to_np(out_s)) and bits_equal(to_np(x["bank"]), to_np(bank_s))
+    assert_close(to_np(plan.out), out_ref, wl.bank_dtype, "readings")
+    assert_close(to_np(x["bank"]), bank_ref, wl.bank_dtype, "bank")
+
+
+def test_decode_plan_checks_steps_before_launching():
+    wl = _wl("bf16", "i32", 4, 64, 128, 8, 8, 1, 4, seed=5)
+    x = workloads.make_decode_inputs(wl, device=DEV)
+    bank0 = x["bank"].clone()
+    plan = sdm.DecodeStepPlan(x["bank"], {k: x[k] for k in DECODE_KEYS})
+    for t0, n, code in ((3, 2, -13), (-1, 1, -13), (4, 1, -13), (0, -1, -7)):
+        with pytest.raises(sdm.SDMError) as e:
+            plan.walk(t0, n)
+        assert e.value.status == code
+    with pytest.raises(sdm.SDMError) as e:
+        plan.launch(4)
+    assert e.value.status == -13
+    plan.walk(4, 0)  # an empty walk past the end launches nothing
+    torch.cuda.synchronize()
+    assert torch.equal(x["bank"].view(torch.int16), bank0.view(torch.int16))  # nothing was launched
+
+
 def test_gather_after_decode_sees_its_writes():
     """A gather launched right after a decode on the same stream (no host synchronisation) reads
     the rows the decode wrote: the overlapped launch waits for its predecessor before reading."""
