@@ -317,6 +317,21 @@ def test_streamed_decode_many_streams_matches_oracle(streams):
     assert sdm.device_status() == 0
 
 
+@pytest.mark.parametrize("streams,W,R,idx", [(16, 256, 256, "i32"), (3, 200, 256, "i64"), (40, 256, 120, "i32")])
+def test_streamed_decode_per_write_gates_and_ragged_passes(streams, W, R, idx):
+    """The streaming kernel with per-write gates (G = W), 32-bit slots, and write / read passes whose
+    last chunk is short (W or R not a multiple of the chunk height), against the oracle."""
+    wl = workloads.DecodeWorkload("wide_gw", "f32", streams, 256, 400, W, R, W, 3, idx, 1 / 16, bank_std=0.5,
+                                  seed=17)
+    x = workloads.make_decode_inputs(wl, device=DEV)
+    bank_ref = to_np(x["bank"])
+    ref = oracle.decode_seq(bank_ref, *(to_np(x[k]) for k in DECODE_KEYS))
+    out = sdm.decode_seq(x["bank"], *(x[k] for k in DECODE_KEYS))
+    torch.cuda.synchronize()
+    assert_close(to_np(out), ref, "f32", "readings")
+    assert_close(to_np(x["bank"]), bank_ref, "f32", "bank")
+
+
 def test_concurrent_calls_on_two_streams_match_sequential():
     """The library keeps no state between calls: a decode of one bank and a gather of another,
     launched on two CUDA streams without synchronising between them, give the same bits as the same
