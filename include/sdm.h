@@ -158,7 +158,8 @@ int sdm_decode_seq_ex(void* bank, const void* k_idx, const float* k_val, const f
 /*
  * Decode-step plan: T single-token steps over time-major inputs, checked once (the decode-side
  * counterpart of the gather launch plan below, for a loop that launches one token at a time, e.g.
- * while serving). sdm_decode_plan_init checks the arguments of sdm_decode_seq(..., T, ...) once
+ * while serving; the pages drive their decode step from such a loop, forward.py, and check each
+ * launch in decode.py's sdm_decode_step). sdm_decode_plan_init checks the arguments of sdm_decode_seq(..., T, ...) once
  * and records the launch of one token; sdm_decode_plan_launch(t) then launches exactly
  * sdm_decode_step on the rows of token t (k_idx + t * n_streams * W, ..., out + t * n_streams * hd),
  * and sdm_decode_plan_walk launches tokens t0 .. t0 + n - 1 in order from one call. The record is
