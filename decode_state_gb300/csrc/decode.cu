@@ -343,8 +343,9 @@ __device__ __forceinline__ void prefetch_rows_l2(const unsigned char* bank, cons
     }
 }
 
-// PIECE = false compiles the per-pair write-back only (the instance for grids of few blocks per SM,
-// where it runs faster without the piece path beside it).
+// PIECE = false compiles the per-pair write-back only; the launcher takes the PIECE instances on
+// every grid (the write-back by pieces measured faster at 2, 3, 4 and 7 blocks per SM), which
+// still fall back to the per-pair path where the pieces do not tile the block's threads.
 // SW (every kernel below): the slice width in columns when it is fixed at compile time, so that
 // the staged rows' addresses in shared memory are immediate offsets; 0 takes it from the arguments.
 template <typename E, typename I, bool PIECE, int SW = 0>
@@ -1407,8 +1408,8 @@ const void* resolve_kernel(int path, bool scalar, const DecodeArgs& a) {
     const auto kernel =
         path == kStaged
             ? ((sizeof(E) == 2 && scalar)
-                   ? (a.piece_write ? vec1_kernel<I, true>(a.slice_cols) : vec1_kernel<I, false>(a.slice_cols))
-                   : (a.piece_write ? vec_kernel<E, I, true>(a.slice_cols) : vec_kernel<E, I, false>(a.slice_cols)))
+                   ? vec1_kernel<I, true>(a.slice_cols)
+                   : vec_kernel<E, I, true>(a.slice_cols))
         : path == kStream ? stream_kernel<E, I>(a.stream_stages, a.slice_cols)
                           : decode_simt_kernel<E, I>;
     return reinterpret_cast<const void*>(kernel);
@@ -1522,9 +1523,10 @@ int plan_decode(const DecodeArgs& a0, int bank_dtype, int idx_dtype, DecodeLaunc
     a.n_slices = (a.hd + sw - 1) / sw;
     const int64_t blocks = a.n_streams * a.n_slices;
     if (blocks > INT_MAX) return SDM_ECOUNT;
-    // decay-and-write by pieces costs one more barrier per token: worth it when the SMs are full
-    // (bandwidth-bound), not when a few blocks per SM wait on latency
-    a.piece_write = blocks >= 4LL * sm_count() ? 1 : 0;
+    // decay-and-write by 16-byte pieces on every grid: one more barrier per token, a quarter of the
+    // per-row stores and address work (serving workload 0.528 vs 0.541 ms, 304 streams 0.334 vs
+    // 0.344, 456 streams 0.367 vs 0.379, the prompt of 64 streams 4.45 vs 4.86 ms)
+    a.piece_write = 1;
     a.stream_rows = kStreamRowsMin;
     a.stream_stages = 4;
     if (streamed && es == 4) {  // float32: the slice geometry of decode_wide_kernel
@@ -1586,9 +1588,6 @@ int plan_decode(const DecodeArgs& a0, int bank_dtype, int idx_dtype, DecodeLaunc
     // wait on latency and gain from the extra warps (full 256-byte rows of many streams keep
     // column pairs: 7 % faster there).
     const bool scalar = (path == kStream && es == 4) || (path == kStaged && es == 2 && sw <= 64);
-    // The one-column kernel writes back by 16-byte pieces on every grid: its per-column path would
-    // store 2 bytes per row and thread (prompt of 64 streams x 1024 tokens: 4.45 instead of 4.86 ms)
-    if (path == kStaged && scalar) a.piece_write = 1;
     const int tcols = scalar ? 1 : cpt;
     const int threads = ((sw + tcols - 1) / tcols + 31) / 32 * 32;
     const size_t smem = path == kStaged ? VecLayout(a.W, a.R, a.G, sw, es, is).total

@@ -26,7 +26,7 @@ struct DecodeArgs {
     int n_slices;     // ceil(hd / slice_cols)
     int stream_rows;    // rows per ring chunk of the streaming path
     int stream_stages;  // chunk buffers in its ring (3 or 4)
-    int piece_write;  // staged path: decay-and-write by 16-byte pieces (many blocks per SM)
+    int piece_write;  // staged path: decay-and-write by 16-byte pieces where they tile the threads
     int inputs_ready; // the inputs predate the preceding kernel: load them before waiting on it
 };
 
