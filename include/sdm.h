@@ -21,7 +21,8 @@
  *     nothing launched); > 0 = the cudaError_t of a failed launch (the error state is consumed).
  *   - Index ranges are the caller's contract: decode slots must lie in the bank, every stream's
  *     slots must be private to it and its W write slots distinct (none of this is checked, as in
- *     the reference). The gather knows the bank's row count and skips out-of-range rows, raising
+ *     the reference). A float32 bank of 64 or more columns is taken to hold fewer than 2^32 rows
+ *     (it would exceed 1 TiB otherwise): its streaming kernel keeps slots as 32-bit row indices. The gather knows the bank's row count and skips out-of-range rows, raising
  *     SDM_DEV_BAD_INDEX in the device status word (sdm_device_status).
  *   - Launches use programmatic stream serialization: a kernel may be scheduled while the previous
  *     kernel on the stream is still finishing, but it reads and writes no memory before that kernel

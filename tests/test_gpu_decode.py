@@ -332,6 +332,23 @@ def test_streamed_decode_per_write_gates_and_ragged_passes(streams, W, R, idx):
     assert_close(to_np(x["bank"]), bank_ref, "f32", "bank")
 
 
+@pytest.mark.parametrize("hd,idx", [(60, "i64"), (64, "i64"), (60, "i32")])
+def test_streamed_decode_slot_widths(hd, idx):
+    """The streaming kernel keeps 64-bit slots as 64-bit row indices for float32 rows of fewer than
+    64 columns and as 32-bit ones from 64 columns on (and for 32-bit slots): rows of 60 and 64
+    columns, W = 256, slots spread over the whole bank, against the oracle."""
+    wl = workloads.DecodeWorkload("wide_slots", "f32", 12, hd, 2000, 256, 96, 256, 3, idx, 1 / 16, bank_std=0.5,
+                                  seed=23)
+    x = workloads.make_decode_inputs(wl, device=DEV)
+    bank_ref = to_np(x["bank"])
+    ref = oracle.decode_seq(bank_ref, *(to_np(x[k]) for k in DECODE_KEYS))
+    out = sdm.decode_seq(x["bank"], *(x[k] for k in DECODE_KEYS))
+    torch.cuda.synchronize()
+    assert_close(to_np(out), ref, "f32", "readings")
+    assert_close(to_np(x["bank"]), bank_ref, "f32", "bank")
+    assert sdm.device_status() == 0
+
+
 def test_concurrent_calls_on_two_streams_match_sequential():
     """The library keeps no state between calls: a decode of one bank and a gather of another,
     launched on two CUDA streams without synchronising between them, give the same bits as the same
