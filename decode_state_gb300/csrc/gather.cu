@@ -96,6 +96,32 @@ __device__ __forceinline__ float weighted_sum(const E* x, int sw, const unsigned
     return acc;
 }
 
+// The weighted sums of two adjacent columns of bf16 rows with bf16 weights (x: the pair's elements
+// of row 0, rows SW elements apart): one 32-bit load per row feeds both chains, so a thread does half
+// the shared-memory loads and weight unpacking per column; each chain runs over ascending entries.
+template <int SW>
+__device__ __forceinline__ float2 weighted_sum_pair_bf16(const uint16_t* x, const unsigned char* wts, int NR) {
+    const uint16_t* w = reinterpret_cast<const uint16_t*>(wts);
+    float a0 = 0.0f, a1 = 0.0f;
+    const auto row = [&](int n, uint16_t wv) {
+        const uint32_t xv = *reinterpret_cast<const uint32_t*>(x + (size_t)n * SW);
+        a0 = fma_bf16(wv, (uint16_t)(xv & 0xffffu), a0);
+        a1 = fma_bf16(wv, (uint16_t)(xv >> 16), a1);
+    };
+    int n = 0;
+    for (; n + 8 <= NR; n += 8) {
+        const uint4 w8 = *reinterpret_cast<const uint4*>(w + n);
+        const uint32_t wp[4] = {w8.x, w8.y, w8.z, w8.w};
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            row(n + 2 * u, (uint16_t)(wp[u] & 0xffffu));
+            row(n + 2 * u + 1, (uint16_t)(wp[u] >> 16));
+        }
+    }
+    for (; n < NR; ++n) row(n, w[n]);
+    return make_float2(a0, a1);
+}
+
 // Zero this block's slice of operand op's output, and for operand 0 its stash rows, of padding
 // token t.
 template <typename E>
@@ -283,8 +309,24 @@ __global__ void __launch_bounds__(kMaxThreads) gather_kernel(const GatherArgs a,
         }
     }
 
-    // the weighted sum, one fmaf chain per column over ascending entries
-    if (active) a.out[op][t * hd + c0 + j] = weighted_sum<E, WT>(rows + j, sw, wt, NR);
+    // the weighted sum, one fmaf chain per column over ascending entries; bf16 rows and weights in
+    // the full 128-column slice take two columns per thread (the first half of the threads):
+    // compact snapshot 0.2764 -> 0.2725 ms, outputs only 0.2231 -> 0.2171 ms, the same bits
+    if constexpr (kRawWeights<E, WT> && SW == kFullSlice) {
+        const int p = 2 * tid;  // this thread's column pair (ncols is a multiple of 8)
+        if (p < ncols) {
+            const float2 r = weighted_sum_pair_bf16<SW>(reinterpret_cast<const uint16_t*>(rows) + p, wt, NR);
+            float* o = a.out[op] + t * hd + c0 + p;
+            if ((reinterpret_cast<uintptr_t>(o) & 7u) == 0) {
+                *reinterpret_cast<float2*>(o) = r;
+            } else {
+                o[0] = r.x;
+                o[1] = r.y;
+            }
+        }
+    } else if (active) {
+        a.out[op][t * hd + c0 + j] = weighted_sum<E, WT>(rows + j, sw, wt, NR);
+    }
     // shared memory must outlive the bulk stores that read it
     if (BULK && stash_rows && stash_bulk && (a.n_slices == 1 ? tid == 0 : tid < 32)) bulk_wait_read_all();
 }

@@ -70,7 +70,8 @@ def test_gather_on_a_misaligned_bank_and_stash():
 def test_gather_aligned_bank_misaligned_stash_and_outputs(wdt):
     """An aligned bank keeps the 16-byte row copies (and the 128-column instance) while the stash and
     the outputs start off a 16-byte boundary: the stash leaves shared memory column by column
-    instead of as one bulk store, and padding tokens zero it the same way."""
+    instead of as one bulk store, and padding tokens zero it the same way; with bf16 weights the
+    column-pair sums meet outputs 4 bytes off an 8-byte boundary and store one float at a time."""
     wl = workloads.GatherWorkload("misaligned_stash", "bf16", 900, 128, 48, 16, (20, 9), "i64", wdt, 0.125, seed=23)
     g = workloads.make_gather_inputs(wl, device=DEV)
     stash = _shifted(torch.full((wl.tokens, wl.widths[0], wl.hd), 3.0, dtype=g["bank"].dtype, device=DEV))
