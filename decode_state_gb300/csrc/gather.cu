@@ -13,9 +13,11 @@
 // operand's entry row slices (all in flight at once) into shared memory; the stash
 // rows then leave shared memory by bulk stores (one cp.async.bulk store for the whole token when
 // the slice is the full row, its lines marked evict-first in L2: the kernel never reads them),
-// while each thread reduces its column over the entries in ascending order with fmaf (the
-// reference's order with one row group). One column per thread (rather than a bf16 pair) gives
-// twice the warps for the reductions; the full gather workload measured 6 % faster that way. The
+// while each column is reduced over the entries in ascending order with fmaf (the reference's
+// order with one row group). The block has a thread per column of the slice, all of which copy
+// rows: whole blocks of column pairs (half the threads) measured 6 % slower. The reduction itself
+// runs one column per thread, except for bf16 rows and weights in the full 128-column slice, where
+// the first half of the threads each sum a column pair (fewer loads and unpackings per column). The
 // row loads use 16-byte copies rather than one bulk copy per row: with 256-byte rows the bulk-copy
 // engine sustained about 3 TB/s of row reads per GPU. Rows that are not a multiple of 16 bytes, or
 // an unaligned bank, take a plain-load path with one column per thread. Row indices outside
