@@ -302,9 +302,9 @@ def test_gather_after_decode_sees_its_writes():
 @pytest.mark.parametrize("streams", [512, 320, 160, 64])
 def test_streamed_decode_many_streams_matches_oracle(streams):
     """Wide rows over grids of several sizes: 1 KiB float32 rows with W = R = 256, which the
-    streaming kernel cuts into whole, half or quarter rows with rings of different depths (chunks of
-    up to 48 rows where few blocks share an SM, two waves of blocks at 320 streams); compared with
-    the oracle on every stream."""
+    streaming kernel cuts into whole, half or quarter rows with rings of different depths (two
+    stages of up to 128 rows where few blocks share an SM, two waves of blocks at 320 streams);
+    compared with the oracle on every stream."""
     wl = workloads.DecodeWorkload("wide_many", "f32", streams, 256, 300, 256, 256, 1, 2, "i64", 1 / 16, bank_std=0.5,
                                   seed=9)
     x = workloads.make_decode_inputs(wl, device=DEV)
