@@ -42,6 +42,8 @@ CASES = [
     ("f32", "bf16", "i64", 1000, 520, 16, 4, (256, 3), True, True),    # widest operand, rows cut into slices
     ("bf16", "bf16", "i32", 700, 13, 24, 6, (5, 7), True, True),       # 26-byte rows: plain-load path
     ("f32", "f32", "i64", 100, 1, 8, 8, (1, 1), True, False),          # head_dim 1, width 1
+    ("bf16", "bf16", "i32", 3000, 136, 64, 16, (13, 21), True, True),  # column pairs, a last slice of 8 columns
+    ("bf16", "bf16", "i64", 2000, 264, 32, 8, (8, 1), False, True),    # three slices; a one-entry operand
 ]
 IDS = [f"{c[0]}-w{c[1]}-{c[2]}-hd{c[4]}-{'x'.join(map(str, c[7]))}-{'stash' if c[8] else 'nostash'}" for c in CASES]
 
@@ -194,6 +196,7 @@ KPOS_CASES = [
     ("bf16", "bf16", "i64", 3000, 128, 128, 16, (32, 32)),
     ("f32", "f32", "i32", 500, 520, 16, 4, (12,)),       # rows cut into slices
     ("bf16", "f32", "i32", 300, 13, 24, 6, (5, 7)),       # 26-byte rows: plain-load path
+    ("bf16", "bf16", "i32", 800, 136, 32, 8, (11, 6)),    # column pairs, a last slice of 8 columns
 ]
 
 
